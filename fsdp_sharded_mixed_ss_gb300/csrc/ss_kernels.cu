@@ -1,0 +1,796 @@
+// ss_kernels.cu -- device side of the shard-step ABI: the virtual-rank gradient
+// reduce, the fused reduce + AdamW + 16-bit cast step, and the unshard /
+// reshard gather copies, with their host-side argument checks and launches.
+//
+// Method ("FSDP: Fully Sharded Data Parallel Training at Scale"): the unit's
+// flat parameter vector is cut into N contiguous shards; in backward the
+// reduce-scatter gives rank k the fp32 sum over ranks of its shard's
+// gradients; the optimizer step then updates the shard's fp32 master, m and v
+// locally; the all-gather concatenates the 16-bit shards into the full unit.
+//
+// Every kernel here is a streaming, HBM-bound pass: no contraction, so no
+// tensor cores. Design for GB300 (sm_103a):
+//   * one thread owns a group of 8 consecutive elements: one 16-byte load per
+//     rank gradient (8 x 16-bit), two 16-byte loads per fp32 state array;
+//     every access is a full 16-byte vector, so each warp moves 512 bytes of
+//     each array per instruction, fully coalesced;
+//   * persistent grid (SM count x resident blocks), grid-stride loop;
+//   * rank gradients are summed in rank order in batches of 8 loads issued
+//     before the adds (8 x 16 B in flight per thread for any N);
+//   * streaming cache hints (evict-first) on read-once and write-once data;
+//   * rank pointer tables travel in the kernel's parameter space
+//     (__grid_constant__), so indexing them costs a constant-bank load;
+//   * odd-length shards and arbitrary views: the first 0..7 elements up to
+//     the common 16-byte phase and the last 0..7 elements are done one by one
+//     by the first threads of the grid; if the arrays do not share a phase the
+//     whole call takes the element-wise kernel (same results).
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ss.h"
+#include "ss_math.cuh"
+
+namespace ss {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroup = 8;         // elements per thread per iteration
+constexpr int kSmallRanks = 64;   // pointer table size of the common kernels
+constexpr int kLargeRanks = SS_MAX_RANKS;
+
+thread_local char g_cuda_err[256] = "";
+
+ss_status cuda_fail(cudaError_t e) {
+  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return SS_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ device helpers
+
+template <int DT>
+__device__ __forceinline__ float widen1(uint16_t h) {
+  if constexpr (DT == SS_BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  else return __half2float(__ushort_as_half(h));
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t narrow1(float x) {
+  if constexpr (DT == SS_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else return __half_as_ushort(__float2half_rn(x));
+}
+
+// Two packed 16-bit values (element 0 in the low half) -> two floats.
+template <int DT>
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+  if constexpr (DT == SS_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  else {
+    __half2 h;
+    std::memcpy(&h, &w, 4);
+    return __half22float2(h);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t narrow2(float a, float b) {
+  uint32_t w;
+  if constexpr (DT == SS_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    std::memcpy(&w, &h, 4);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    std::memcpy(&w, &h, 4);
+  }
+  return w;
+}
+
+template <int DT>
+__device__ __forceinline__ void widen8(const uint4& w, float (&f)[8]) {
+  float2 a = widen2<DT>(w.x), b = widen2<DT>(w.y), c = widen2<DT>(w.z), d = widen2<DT>(w.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <int DT>
+__device__ __forceinline__ void add8(const uint4& w, float (&f)[8]) {
+  float t[8];
+  widen8<DT>(w, t);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = f[j] + t[j];
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 narrow8(const float (&f)[8]) {
+  return make_uint4(narrow2<DT>(f[0], f[1]), narrow2<DT>(f[2], f[3]), narrow2<DT>(f[4], f[5]),
+                    narrow2<DT>(f[6], f[7]));
+}
+
+__device__ __forceinline__ void ld8f(const float* p, float (&f)[8]) {
+  float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void st8f(float* p, const float (&f)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(f[0], f[1], f[2], f[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+}
+
+__device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
+
+// ------------------------------------------------------------------ argument blocks
+
+template <int MAXR>
+struct RankTable {
+  const void* p[MAXR];
+};
+
+template <int MAXR>
+struct StepArgs {
+  RankTable<MAXR> ranks;
+  const float* g32;
+  float* master;
+  float* m;
+  float* v;
+  void* p16;
+  float* g_out;
+  int32_t* nonfinite;
+  const float* dev_scale;
+  const int32_t* dev_skip;
+  int64_t n;
+  int64_t head;  // elements before the first 16-byte-aligned group (vector kernel only)
+  int32_t n_ranks;
+  float post_scale;
+  AdamConst k;
+};
+
+template <int MAXR>
+struct ReduceArgs {
+  RankTable<MAXR> ranks;
+  float* out;
+  int32_t* nonfinite;
+  int64_t n;
+  int64_t head;
+  int32_t n_ranks;
+  float post_scale;
+  int32_t accumulate;
+};
+
+// Sum of the ranks' 8 elements starting at e, in rank order, fp32.
+template <int GT, int MAXR>
+__device__ __forceinline__ void reduce8(const RankTable<MAXR>& t, int n_ranks, int64_t e, float (&g)[8]) {
+  for (int r0 = 0; r0 < n_ranks; r0 += 8) {
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (r0 + j < n_ranks) w[j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(t.p[r0 + j]) + e));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j < n_ranks) {
+        if (r0 + j == 0) widen8<GT>(w[j], g);
+        else add8<GT>(w[j], g);
+      }
+    }
+  }
+}
+
+template <int GT, int MAXR>
+__device__ __forceinline__ float reduce1(const RankTable<MAXR>& t, int n_ranks, int64_t e) {
+  float acc = widen1<GT>(static_cast<const uint16_t*>(t.p[0])[e]);
+  for (int r = 1; r < n_ranks; ++r) acc = acc + widen1<GT>(static_cast<const uint16_t*>(t.p[r])[e]);
+  return acc;
+}
+
+// ------------------------------------------------------------------ fused AdamW step
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float gs, bool& bad) {
+  float g;
+  if constexpr (FROM_G32) {
+    g = a.g32[e];
+  } else {
+    g = reduce1<GT>(a.ranks, a.n_ranks, e);
+    if (a.post_scale != 1.0f) g = g * a.post_scale;
+  }
+  bad |= !finite(g);
+  if (a.g_out) a.g_out[e] = g;
+  if (a.dev_scale) g = g * gs;
+  float p = a.master[e], m = a.m[e], v = a.v[e];
+  adamw_elem(a.k, g, p, m, v);
+  a.master[e] = p;
+  a.m[e] = m;
+  a.v[e] = v;
+  if constexpr (WRITE_P16) static_cast<uint16_t*>(a.p16)[e] = narrow1<PT>(p);
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kThreads) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (FROM_G32) {
+      ld8f(a.g32 + e, g);
+    } else {
+      reduce8<GT>(a.ranks, a.n_ranks, e, g);
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8], m[8], v[8];
+    ld8f(a.master + e, p);
+    ld8f(a.m + e, m);
+    ld8f(a.v + e, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+  }
+  // the (< 8) elements before the aligned body and the (< 8) after it
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) {
+    const int64_t e = tid < a.head ? tid : tail0 + (tid - a.head);
+    step1<GT, PT, FROM_G32, WRITE_P16>(a, e, gs, bad);
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t e = tid; e < a.n; e += stride) step1<GT, PT, FROM_G32, WRITE_P16>(a, e, gs, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// ------------------------------------------------------------------ gradient reduce
+
+template <int GT, int MAXR>
+__device__ __forceinline__ void reduce_one(const ReduceArgs<MAXR>& a, int64_t e, bool& bad) {
+  float g = reduce1<GT>(a.ranks, a.n_ranks, e);
+  if (a.post_scale != 1.0f) g = g * a.post_scale;
+  if (a.accumulate) g = a.out[e] + g;
+  bad |= !finite(g);
+  a.out[e] = g;
+}
+
+template <int GT, int MAXR>
+__global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    reduce8<GT>(a.ranks, a.n_ranks, e, g);
+    if (a.post_scale != 1.0f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+    }
+    if (a.accumulate) {
+      float o[8];
+      ld8f(a.out + e, o);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = o[j] + g[j];
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    st8f(a.out + e, g);
+  }
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) reduce_one<GT>(a, tid < a.head ? tid : tail0 + (tid - a.head), bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int GT, int MAXR>
+__global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t e = tid; e < a.n; e += stride) reduce_one<GT>(a, e, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// ------------------------------------------------------------------ unshard / reshard copies
+
+template <int MAXR>
+struct CopyArgs {
+  const void* src[MAXR];
+  void* dst[MAXR];
+  int64_t bytes[MAXR];
+  int32_t n_seg;
+  int32_t esize;
+};
+
+// 16 bytes starting SOFF bytes into the 32-byte window (c0, c1).
+template <int SOFF>
+__device__ __forceinline__ uint4 window16(const uint4& c0, const uint4& c1) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  constexpr int q = SOFF / 4;
+  constexpr int r = SOFF % 4;
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (r == 0) o[i] = w[q + i];
+    else o[i] = __funnelshift_r(w[q + i], w[q + i + 1], 8 * r);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Body of one segment: destination-aligned 16-byte vectors. The source of
+// vector j starts SOFF bytes past a 16-byte boundary; misaligned sources are
+// read as the two aligned 16-byte chunks that hold it, and only when both
+// chunks lie inside the source range -- otherwise element by element.
+template <int SOFF>
+__device__ __forceinline__ void copy_body(const char* s, char* d, int64_t h, int64_t nvec, int64_t bytes, int esize,
+                                          int64_t tid, int64_t stride) {
+  for (int64_t j = tid; j < nvec; j += stride) {
+    const int64_t off = h + 16 * j;  // byte offset of this vector in the segment
+    uint4* dv = reinterpret_cast<uint4*>(d + off);
+    if constexpr (SOFF == 0) {
+      __stcs(dv, __ldcs(reinterpret_cast<const uint4*>(s + off)));
+    } else {
+      const char* c0 = s + off - SOFF;
+      if (c0 >= s && (off - SOFF) + 32 <= bytes) {
+        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(c0));
+        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(c0 + 16));
+        __stcs(dv, window16<SOFF>(a, b));
+      } else {
+        for (int i = 0; i < 16; i += esize) {
+          if (esize == 2) *reinterpret_cast<uint16_t*>(d + off + i) = *reinterpret_cast<const uint16_t*>(s + off + i);
+          else *reinterpret_cast<uint32_t*>(d + off + i) = *reinterpret_cast<const uint32_t*>(s + off + i);
+        }
+      }
+    }
+  }
+}
+
+template <int MAXR>
+__global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_constant__ CopyArgs<MAXR> a) {
+  const int k = blockIdx.y;
+  const int64_t bytes = a.bytes[k];
+  if (bytes == 0) return;
+  const char* s = static_cast<const char*>(a.src[k]);
+  char* d = static_cast<char*>(a.dst[k]);
+  int64_t h = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u);
+  if (h > bytes) h = bytes;
+  const int64_t nvec = (bytes - h) >> 4;
+  const int64_t t0 = h + (nvec << 4);
+  const int soff = static_cast<int>(reinterpret_cast<uintptr_t>(s + h) & 15u);
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  switch (soff) {
+    case 0: copy_body<0>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 2: copy_body<2>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 4: copy_body<4>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 6: copy_body<6>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 8: copy_body<8>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 10: copy_body<10>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 12: copy_body<12>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    default: copy_body<14>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+  }
+  // head (h bytes) and tail (bytes - t0) element by element
+  const int64_t nh = h / a.esize, nt = (bytes - t0) / a.esize;
+  if (tid < nh + nt) {
+    const int64_t off = tid < nh ? tid * a.esize : t0 + (tid - nh) * a.esize;
+    if (a.esize == 2) *reinterpret_cast<uint16_t*>(d + off) = *reinterpret_cast<const uint16_t*>(s + off);
+    else *reinterpret_cast<uint32_t*>(d + off) = *reinterpret_cast<const uint32_t*>(s + off);
+  }
+}
+
+// ------------------------------------------------------------------ host helpers
+
+struct Range {
+  uintptr_t lo, hi;
+  bool out;
+};
+
+// True when some output byte range overlaps any other range (inputs may overlap inputs).
+bool any_output_overlap(std::vector<Range>& rs) {
+  rs.erase(std::remove_if(rs.begin(), rs.end(), [](const Range& r) { return r.hi <= r.lo; }), rs.end());
+  std::sort(rs.begin(), rs.end(), [](const Range& x, const Range& y) { return x.lo < y.lo; });
+  uintptr_t max_out = 0, max_any = 0;
+  for (const Range& r : rs) {
+    if (r.lo < max_out) return true;
+    if (r.out && r.lo < max_any) return true;
+    max_any = std::max(max_any, r.hi);
+    if (r.out) max_out = std::max(max_out, r.hi);
+  }
+  return false;
+}
+
+Range rng(const void* p, int64_t bytes, bool out) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return {a, a + static_cast<uintptr_t>(bytes), out};
+}
+
+// Smallest h in [0, 8) with every 16-bit pointer at a 16-byte boundary after h
+// elements and every fp32 pointer likewise; -1 when none exists.
+int common_phase(const std::vector<uintptr_t>& p16, const std::vector<uintptr_t>& p32) {
+  for (int h = 0; h < 8; ++h) {
+    bool ok = true;
+    for (uintptr_t p : p16) ok = ok && ((p + 2u * h) & 15u) == 0;
+    for (uintptr_t p : p32) ok = ok && ((p + 4u * h) & 15u) == 0;
+    if (ok) return h;
+  }
+  return -1;
+}
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+// Resident blocks per SM of a kernel (cached per kernel).
+int blocks_per_sm(const void* fn) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  for (auto& c : cache)
+    if (c.first == fn) return c.second;
+  int b = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, 0) != cudaSuccess || b < 1) b = 1;
+  cache.emplace_back(fn, b);
+  return b;
+}
+
+unsigned grid_for(const void* fn, int64_t work_items) {
+  const int64_t want = std::max<int64_t>(1, (work_items + kThreads - 1) / kThreads);
+  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(fn));
+  return static_cast<unsigned>(std::min(want, cap));
+}
+
+template <typename Args, typename Fn>
+ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream) {
+  fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+bool is16(ss_dtype d) { return d == SS_BF16 || d == SS_FP16; }
+
+AdamConst make_const(const ss_adamw_hparams& hp) {
+  const double b1 = hp.beta1, b2 = hp.beta2;
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp.step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(hp.step));
+  const double S = static_cast<double>(hp.lr) / bc1;
+  const double R = 1.0 / std::sqrt(bc2);
+  const double L = static_cast<double>(hp.lr) * static_cast<double>(hp.weight_decay);
+  const double c1 = 1.0 - b1, c2 = 1.0 - b2;
+  AdamConst k;
+  k.b1 = hp.beta1;
+  k.c1 = static_cast<float>(c1);
+  k.c1_lo = static_cast<float>(c1 - static_cast<double>(k.c1));
+  k.b2 = hp.beta2;
+  k.c2 = static_cast<float>(c2);
+  k.c2_lo = static_cast<float>(c2 - static_cast<double>(k.c2));
+  k.eps = hp.eps;
+  k.S_hi = static_cast<float>(S);
+  k.S_lo = static_cast<float>(S - static_cast<double>(k.S_hi));
+  k.R_hi = static_cast<float>(R);
+  k.R_lo = static_cast<float>(R - static_cast<double>(k.R_hi));
+  k.L_hi = static_cast<float>(L);
+  k.L_lo = static_cast<float>(L - static_cast<double>(k.L_hi));
+  return k;
+}
+
+bool valid_hp(const ss_adamw_hparams* hp) {
+  if (!hp || hp->step < 1) return false;
+  const float f[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  for (float x : f)
+    if (!std::isfinite(x) || x < 0.0f) return false;
+  return hp->beta1 < 1.0f && hp->beta2 < 1.0f;
+}
+
+// ---- dispatch tables (template instantiation by runtime dtype / options)
+
+template <int MAXR>
+ss_status run_adam(const StepArgs<MAXR>& a, bool vec, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
+                   void* stream) {
+#define SS_ADAM_CASE(G, P, F, W)                                                          \
+  if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
+    if (vec) {                                                                            \
+      auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                       \
+      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
+    }                                                                                     \
+    auto* fn = adam_scalar_kernel<G, P, F, W, MAXR>;                                      \
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), a.n), a, stream);       \
+  }
+#define SS_ADAM_P(G, P) SS_ADAM_CASE(G, P, false, true) SS_ADAM_CASE(G, P, false, false) \
+                        SS_ADAM_CASE(G, P, true, true) SS_ADAM_CASE(G, P, true, false)
+  SS_ADAM_P(SS_BF16, SS_BF16)
+  SS_ADAM_P(SS_BF16, SS_FP16)
+  SS_ADAM_P(SS_FP16, SS_BF16)
+  SS_ADAM_P(SS_FP16, SS_FP16)
+#undef SS_ADAM_P
+#undef SS_ADAM_CASE
+  return SS_ERR_DTYPE;
+}
+
+template <int MAXR>
+ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* stream) {
+#define SS_RED_CASE(G)                                                                     \
+  if (gt == G) {                                                                           \
+    if (vec) {                                                                             \
+      auto* fn = reduce_vec_kernel<G, MAXR>;                                               \
+      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
+    }                                                                                      \
+    auto* fn = reduce_scalar_kernel<G, MAXR>;                                              \
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), a.n), a, stream);        \
+  }
+  SS_RED_CASE(SS_BF16)
+  SS_RED_CASE(SS_FP16)
+#undef SS_RED_CASE
+  return SS_ERR_DTYPE;
+}
+
+template <int MAXR>
+ss_status run_copy(const void* const* src, void* const* dst, const int64_t* bytes, int32_t n_seg, int32_t esize,
+                   int64_t total_bytes, void* stream) {
+  CopyArgs<MAXR> a;
+  std::memset(&a, 0, sizeof a);
+  for (int32_t k = 0; k < n_seg; ++k) {
+    a.src[k] = src[k];
+    a.dst[k] = dst[k];
+    a.bytes[k] = bytes[k];
+  }
+  a.n_seg = n_seg;
+  a.esize = esize;
+  auto* fn = copy_segments_kernel<MAXR>;
+  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(fn)));
+  const int64_t per_seg_work = (total_bytes / std::max(1, n_seg)) / 16 + 1;
+  int64_t gx = std::min<int64_t>((cap + n_seg - 1) / n_seg, (per_seg_work + kThreads - 1) / kThreads);
+  gx = std::max<int64_t>(gx, 1);
+  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg));
+  fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(a);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+ss_status check_ranks(const void* const* rank_grads, int32_t n_ranks, ss_dtype gdtype, int64_t n,
+                      std::vector<Range>& ranges, std::vector<uintptr_t>& p16) {
+  if (!rank_grads || n_ranks < 1 || n_ranks > SS_MAX_RANKS) return SS_ERR_INVALID_ARG;
+  if (!is16(gdtype)) return SS_ERR_DTYPE;
+  for (int32_t r = 0; r < n_ranks; ++r) {
+    if (!rank_grads[r]) return SS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(rank_grads[r]) & 1u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(rank_grads[r], 2 * n, false));
+    p16.push_back(reinterpret_cast<uintptr_t>(rank_grads[r]));
+  }
+  return SS_OK;
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+const char* ss_last_cuda_error(void) { return g_cuda_err; }
+
+ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtype gdtype, int64_t n,
+                         float post_scale, int32_t accumulate, float* g_out, int32_t* nonfinite_flag,
+                         void* stream) {
+  if (n < 0) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+  if (st != SS_OK) return st;
+  if (!g_out) return SS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(g_out) & 3u) return SS_ERR_ALIGN;
+  if (nonfinite_flag && (reinterpret_cast<uintptr_t>(nonfinite_flag) & 3u)) return SS_ERR_ALIGN;
+  ranges.push_back(rng(g_out, 4 * n, true));
+  if (nonfinite_flag) ranges.push_back(rng(nonfinite_flag, 4, true));
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  if (n == 0) return SS_OK;
+  p32.push_back(reinterpret_cast<uintptr_t>(g_out));
+  const int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  auto fill = [&](auto& a) {
+    for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.out = g_out;
+    a.nonfinite = nonfinite_flag;
+    a.n = n;
+    a.head = vec ? h : 0;
+    a.n_ranks = n_ranks;
+    a.post_scale = post_scale;
+    a.accumulate = accumulate != 0;
+  };
+  if (n_ranks <= kSmallRanks) {
+    ReduceArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_reduce(a, vec, gdtype, stream);
+  }
+  ReduceArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_reduce(a, vec, gdtype, stream);
+}
+
+ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, const void* const* rank_grads,
+                       int32_t n_ranks, ss_dtype gdtype, float post_scale, float* master, float* m, float* v,
+                       void* param16, ss_dtype pdtype, const ss_step_options* opts, void* stream) {
+  if (!valid_hp(hp) || n < 0) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  if (!master || !m || !v) return SS_ERR_INVALID_ARG;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  const bool from_g32 = g32 != nullptr;
+  if (from_g32) {
+    if (reinterpret_cast<uintptr_t>(g32) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g32, 4 * n, false));
+    p32.push_back(reinterpret_cast<uintptr_t>(g32));
+  } else {
+    ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+    if (st != SS_OK) return st;
+  }
+  for (const float* p : {static_cast<const float*>(master), static_cast<const float*>(m), static_cast<const float*>(v)}) {
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(p, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(p));
+  }
+  if (param16) {
+    if (!is16(pdtype)) return SS_ERR_DTYPE;
+    if (reinterpret_cast<uintptr_t>(param16) & 1u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(param16, 2 * n, true));
+    p16.push_back(reinterpret_cast<uintptr_t>(param16));
+  }
+  ss_step_options o{};
+  if (opts) o = *opts;
+  if (o.g_out) {
+    if (reinterpret_cast<uintptr_t>(o.g_out) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.g_out, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(o.g_out));
+  }
+  if (o.nonfinite_flag) {
+    if (reinterpret_cast<uintptr_t>(o.nonfinite_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.nonfinite_flag, 4, true));
+  }
+  if (o.dev_grad_scale) {
+    if (reinterpret_cast<uintptr_t>(o.dev_grad_scale) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.dev_grad_scale, 4, false));
+  }
+  if (o.dev_skip_flag) {
+    if (reinterpret_cast<uintptr_t>(o.dev_skip_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.dev_skip_flag, 4, false));
+  }
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  if (n == 0) return SS_OK;
+  const int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  const AdamConst k = make_const(*hp);
+  auto fill = [&](auto& a) {
+    if (!from_g32)
+      for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.g32 = g32;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.p16 = param16;
+    a.g_out = o.g_out;
+    a.nonfinite = o.nonfinite_flag;
+    a.dev_scale = o.dev_grad_scale;
+    a.dev_skip = o.dev_skip_flag;
+    a.n = n;
+    a.head = vec ? h : 0;
+    a.n_ranks = from_g32 ? 0 : n_ranks;
+    a.post_scale = post_scale;
+    a.k = k;
+  };
+  const ss_dtype gt = from_g32 ? SS_BF16 : gdtype;
+  const ss_dtype pt = param16 ? pdtype : SS_BF16;
+  if (from_g32 || n_ranks <= kSmallRanks) {
+    StepArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_adam(a, vec, from_g32, param16 != nullptr, gt, pt, stream);
+  }
+  StepArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_adam(a, vec, from_g32, param16 != nullptr, gt, pt, stream);
+}
+
+static ss_status copy_common(const void* const* src, void* const* dst, const int64_t* shard_bounds, int32_t n_ranks,
+                             ss_dtype dtype, bool unshard, void* stream) {
+  if (!shard_bounds || n_ranks < 1 || n_ranks > SS_MAX_RANKS) return SS_ERR_INVALID_ARG;
+  if (dtype != SS_BF16 && dtype != SS_FP16 && dtype != SS_FP32) return SS_ERR_DTYPE;
+  const int32_t es = dtype == SS_FP32 ? 4 : 2;
+  if (shard_bounds[0] != 0) return SS_ERR_INVALID_ARG;
+  for (int32_t k = 0; k < n_ranks; ++k)
+    if (shard_bounds[k + 1] < shard_bounds[k]) return SS_ERR_INVALID_ARG;
+  const int64_t P = shard_bounds[n_ranks];
+  if (P > INT64_MAX / 8) return SS_ERR_OVERFLOW;
+  std::vector<const void*> s(n_ranks);
+  std::vector<void*> d(n_ranks);
+  std::vector<int64_t> b(n_ranks);
+  std::vector<Range> ranges;
+  const void* flat = unshard ? static_cast<const void*>(dst[0]) : src[0];
+  if (!flat && P > 0) return SS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(flat) % es) return SS_ERR_ALIGN;
+  ranges.push_back(rng(flat, es * P, unshard));
+  for (int32_t k = 0; k < n_ranks; ++k) {
+    const int64_t len = shard_bounds[k + 1] - shard_bounds[k];
+    const void* shard = unshard ? src[k + 1] : static_cast<const void*>(dst[k + 1]);
+    if (len > 0 && !shard) return SS_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(shard) % es) return SS_ERR_ALIGN;
+    ranges.push_back(rng(shard, es * len, !unshard));
+    char* fk = static_cast<char*>(const_cast<void*>(flat)) + es * shard_bounds[k];
+    s[k] = unshard ? shard : fk;
+    d[k] = unshard ? static_cast<void*>(fk) : const_cast<void*>(shard);
+    b[k] = es * len;
+  }
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  if (P == 0) return SS_OK;
+  if (n_ranks <= kSmallRanks) return run_copy<kSmallRanks>(s.data(), d.data(), b.data(), n_ranks, es, es * P, stream);
+  return run_copy<kLargeRanks>(s.data(), d.data(), b.data(), n_ranks, es, es * P, stream);
+}
+
+ss_status ss_unshard(const void* const* shards, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
+                     void* flat, void* stream) {
+  if (!shards || n_ranks < 1 || n_ranks > SS_MAX_RANKS) return SS_ERR_INVALID_ARG;
+  std::vector<const void*> src(n_ranks + 1);
+  std::vector<void*> dst(n_ranks + 1);
+  dst[0] = flat;
+  for (int32_t k = 0; k < n_ranks; ++k) src[k + 1] = shards[k];
+  return copy_common(src.data(), dst.data(), shard_bounds, n_ranks, dtype, true, stream);
+}
+
+ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
+                     void* const* shards, void* stream) {
+  if (!shards || n_ranks < 1 || n_ranks > SS_MAX_RANKS) return SS_ERR_INVALID_ARG;
+  std::vector<const void*> src(n_ranks + 1);
+  std::vector<void*> dst(n_ranks + 1);
+  src[0] = flat;
+  for (int32_t k = 0; k < n_ranks; ++k) dst[k + 1] = shards[k];
+  return copy_common(src.data(), dst.data(), shard_bounds, n_ranks, dtype, false, stream);
+}
+
+}  // extern "C"

@@ -26,3 +26,24 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_libraries():
+    """Build whatever library is missing (the oracle, the generator, the CUDA library)."""
+    import importlib.util
+
+    import oracle
+    import synth
+
+    if not os.path.exists(oracle._SO):
+        oracle.build()
+    if not (os.path.exists(synth._HOST_SO) and os.path.exists(synth._DEV_SO)):
+        synth.build()
+    lib = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "libss.so")
+    if not os.path.exists(lib):
+        spec = importlib.util.spec_from_file_location("ss_build", os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "_build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
+    yield

@@ -1,0 +1,263 @@
+"""GPU edge cases of each kernel through the C ABI, against the oracle.
+
+Reduce: bit-exact for any rank count (1..1024), ragged lengths, both 16-bit
+formats, misaligned views (element-wise kernel), post_scale, accumulation and
+the non-finite flag; a rank-order probe. AdamW: misaligned views and odd
+lengths, the fp32-gradient entry, the optional outputs and device-side
+controls (g_out, non-finite flag, gradient scale, skip flag). Unshard/reshard:
+bit-exact for empty shards, P < N, odd offsets (shifted-source path), fp32,
+and N = 1024.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+from parity import assert_p16_within_ulp, assert_state_close
+
+pytestmark = pytest.mark.gpu
+
+HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=3)
+
+
+@pytest.fixture(scope="module")
+def ss():
+    import fsdp_sharded_mixed_ss_gb300 as m
+    return m
+
+
+def tdt(fmt):
+    import torch
+    return {synth.BF16: torch.bfloat16, synth.FP16: torch.float16}[fmt]
+
+
+def dev_bits(spec, n, offset=0, pad=0):
+    """Device buffer of n generated elements, viewed `offset` elements into a larger allocation."""
+    import torch
+    dt = torch.float32 if spec.fmt == synth.FP32 else tdt(spec.fmt)
+    base = torch.zeros(n + offset + pad, dtype=dt, device="cuda")
+    view = base[offset:offset + n]
+    if n:
+        synth.device_fill(spec, view.view(torch.int32 if spec.fmt == synth.FP32 else torch.int16))
+    return view
+
+
+def host_bits(spec, n):
+    return synth.host_range(spec, 0, n)
+
+
+def bits_of(t):
+    import torch
+    if t.dtype == torch.float32:
+        return t.cpu().numpy()
+    return t.view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ----------------------------------------------------------------------------- reduce
+
+@pytest.mark.parametrize("N", [1, 2, 3, 8, 64, 65, 1024])
+@pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
+def test_reduce_bit_exact(ss, N, fmt):
+    import torch
+    n = 4099 if N < 1000 else 1000
+    specs = [synth.normal(1e-3, fmt, synth.GRAD, r, 1) if fmt == synth.BF16 else synth.uniform(6e-5, fmt, synth.GRAD, r, 1)
+             for r in range(N)]
+    G = [dev_bits(s, n) for s in specs]
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    ss.ss_grad_reduce(G, n, out)
+    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], fmt)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+@pytest.mark.parametrize("offsets", [(0, 0), (1, 0), (0, 1), (3, 5), (7, 7)])
+def test_reduce_views_scale_accumulate_flag(ss, offsets):
+    import torch
+    go, oo = offsets
+    N, n = 8, 100_003
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 2) for r in range(N)]
+    G = [dev_bits(s, n, offset=go) for s in specs]
+    base = torch.zeros(n + oo, dtype=torch.float32, device="cuda")
+    out = base[oo:]
+    init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
+    out.copy_(init)
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ss.ss_grad_reduce(G, n, out, post_scale=0.125, accumulate=True, nonfinite_flag=flag)
+    acc = bits_of(init).copy()
+    oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, post_scale=0.125, accumulate_into=acc)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+    assert flag.item() == 0
+    G[5][n // 2] = float("inf")
+    ss.ss_grad_reduce(G, n, out, nonfinite_flag=flag)
+    assert flag.item() == 1
+
+
+def test_reduce_rank_order_probe(ss):
+    import torch
+    vals = torch.tensor([2.0 ** 27, 1.0, -2.0 ** 27], dtype=torch.bfloat16, device="cuda")
+    n = 40
+    G = [torch.full((n,), float(v), dtype=torch.bfloat16, device="cuda") for v in vals.float().tolist()]
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    ss.ss_grad_reduce(G, n, out)
+    assert (out == 0).all()
+    ss.ss_grad_reduce([G[0], G[2], G[1]], n, out)
+    assert (out == 1).all()
+
+
+# ----------------------------------------------------------------------------- AdamW step
+
+def _state(n, off=0):
+    return (dev_bits(synth.normal(0.02, synth.FP32, synth.MASTER), n, off),
+            dev_bits(synth.normal(1e-4, synth.FP32, synth.MOM1), n, off),
+            dev_bits(synth.normal(1e-8, synth.FP32, synth.MOM2, absolute=True), n, off))
+
+
+def _oracle_step(n, N, fmt, hp, grad_scale=1.0, post_scale=1.0):
+    specs = [synth.normal(1e-3, fmt, synth.GRAD, r, 9) for r in range(N)]
+    master = host_bits(synth.normal(0.02, synth.FP32, synth.MASTER), n).view(np.float32).copy()
+    m = host_bits(synth.normal(1e-4, synth.FP32, synth.MOM1), n).view(np.float32).copy()
+    v = host_bits(synth.normal(1e-8, synth.FP32, synth.MOM2, absolute=True), n).view(np.float32).copy()
+    g = oracle.grad_reduce([host_bits(s, n) for s in specs], fmt, post_scale=post_scale)
+    p16 = oracle.adamw(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], hp["step"], g, master, m, v,
+                       p16_dtype=fmt, grad_scale=grad_scale)
+    return specs, g, master, m, v, p16
+
+
+def _check(master, m, v, p16, ref, fmt):
+    _, _, rm, rmm, rv, rp = ref
+    assert_state_close(bits_of(master), rm, "master")
+    assert_state_close(bits_of(m), rmm, "m")
+    assert_state_close(bits_of(v), rv, "v")
+    assert_p16_within_ulp(bits_of(p16), rp, fmt, "p16")
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 9, 4099, 100_003])
+@pytest.mark.parametrize("goff,soff,poff", [(0, 0, 0), (1, 1, 1), (2, 0, 0), (0, 3, 0), (5, 2, 4), (0, 0, 3)])
+def test_step_odd_lengths_and_views(ss, n, goff, soff, poff):
+    import torch
+    N, fmt = 4, synth.BF16
+    ref = _oracle_step(n, N, fmt, HP)
+    G = [dev_bits(s, n, goff) for s in ref[0]]
+    master, m, v = _state(n, soff)
+    p16 = torch.zeros(n + poff, dtype=tdt(fmt), device="cuda")[poff:]
+    ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16)
+    _check(master, m, v, p16, ref, fmt)
+
+
+@pytest.mark.parametrize("N", [1, 2, 9, 64, 130])
+@pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
+def test_step_rank_counts(ss, N, fmt):
+    import torch
+    n = 20_011
+    ref = _oracle_step(n, N, fmt, HP)
+    G = [dev_bits(s, n) for s in ref[0]]
+    master, m, v = _state(n)
+    p16 = torch.zeros(n, dtype=tdt(fmt), device="cuda")
+    ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16)
+    _check(master, m, v, p16, ref, fmt)
+
+
+def test_step_from_fp32_grad_matches_fused(ss):
+    import torch
+    n, N = 50_001, 8
+    ref = _oracle_step(n, N, synth.BF16, HP)
+    G = [dev_bits(s, n) for s in ref[0]]
+    g32 = torch.empty(n, dtype=torch.float32, device="cuda")
+    ss.ss_grad_reduce(G, n, g32)
+    master, m, v = _state(n)
+    p16 = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(HP, n, master, m, v, g32=g32, param16=p16)
+    _check(master, m, v, p16, ref, synth.BF16)
+    # the two-kernel path and the fused path write identical bits
+    master2, m2, v2 = _state(n)
+    p2 = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(HP, n, master2, m2, v2, rank_grads=G, param16=p2)
+    for a, b in ((master, master2), (m, m2), (v, v2)):
+        assert torch.equal(a, b)
+    assert torch.equal(p16.view(torch.int16), p2.view(torch.int16))
+
+
+def test_step_options(ss):
+    import torch
+    n, N = 30_001, 4
+    coef = np.float32(0.37)
+    ref = _oracle_step(n, N, synth.BF16, HP, grad_scale=float(coef), post_scale=0.25)
+    G = [dev_bits(s, n) for s in ref[0]]
+    master, m, v = _state(n)
+    p16 = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    g_out = torch.empty(n, dtype=torch.float32, device="cuda")
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = torch.tensor([coef], dtype=torch.float32, device="cuda")
+    skip = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, post_scale=0.25, param16=p16, g_out=g_out,
+                    nonfinite_flag=flag, dev_grad_scale=scale, dev_skip_flag=skip)
+    _check(master, m, v, p16, ref, synth.BF16)
+    assert np.array_equal(g_out.cpu().numpy().view(np.uint32), ref[1].view(np.uint32))
+    assert flag.item() == 0
+    # skip flag set: nothing is written
+    before = [t.clone() for t in (master, m, v, p16)]
+    skip.fill_(1)
+    G[1][77] = float("nan")
+    ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16, nonfinite_flag=flag, dev_skip_flag=skip)
+    for a, b in zip(before, (master, m, v, p16)):
+        assert torch.equal(a.view(torch.int16) if a.dtype != torch.float32 else a,
+                           b.view(torch.int16) if b.dtype != torch.float32 else b)
+    assert flag.item() == 0
+    skip.fill_(0)
+    ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16, nonfinite_flag=flag, dev_skip_flag=skip)
+    assert flag.item() == 1
+
+
+def test_step_writes_into_flat_buffer(ss):
+    """param16 may point into the flat unit buffer at the shard's offset (fused unshard)."""
+    import torch
+    P, N = 100_000, 7
+    _, bounds = ss.ss_flatten_layout([P], N)
+    flat = torch.zeros(P, dtype=torch.bfloat16, device="cuda")
+    for k in range(N):
+        lo, hi = int(bounds[k]), int(bounds[k + 1])
+        n = hi - lo
+        ref = _oracle_step(n, 2, synth.BF16, HP)
+        G = [dev_bits(s, n) for s in ref[0]]
+        master, m, v = _state(n)
+        ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=flat[lo:hi])
+        _check(master, m, v, flat[lo:hi], ref, synth.BF16)
+
+
+# ----------------------------------------------------------------------------- unshard / reshard
+
+@pytest.mark.parametrize("P,N", [(0, 3), (2, 5), (100, 3), (4099, 64), (1_000_003, 8), (123_457, 1024)])
+@pytest.mark.parametrize("fmt", [synth.BF16, synth.FP32])
+def test_unshard_reshard_exact(ss, P, N, fmt):
+    import torch
+    _, b = ss.ss_flatten_layout([P], N)
+    dt = torch.float32 if fmt == synth.FP32 else torch.bfloat16
+    shards = []
+    for k in range(N):
+        n = int(b[k + 1] - b[k])
+        shards.append(dev_bits(synth.normal(1.0, fmt, synth.PARAM16, k), n, offset=k % 3))
+    flat = torch.full((P,), -1.0, dtype=dt, device="cuda")
+    ss.ss_unshard(shards, b, flat)
+    host = [bits_of(s) for s in shards]
+    expect = oracle.unshard(host, b) if P else np.zeros(0)
+    got = bits_of(flat)
+    assert np.array_equal(got.view(np.uint8), expect.view(np.uint8))
+    back = [torch.full((int(b[k + 1] - b[k]) + 3,), 7.0, dtype=dt, device="cuda")[(k * 5) % 4:][:int(b[k + 1] - b[k])]
+            for k in range(N)]
+    ss.ss_reshard(flat, b, back)
+    for x, y in zip(back, host):
+        assert np.array_equal(bits_of(x).view(np.uint8), y.view(np.uint8))
+
+
+def test_unshard_into_offset_flat(ss):
+    """The flat buffer itself at odd element offsets: every shard lands on a shifted boundary."""
+    import torch
+    P, N = 65_537, 8
+    _, b = ss.ss_flatten_layout([P], N)
+    for off in range(8):
+        shards = [dev_bits(synth.normal(1.0, synth.FP16, synth.PARAM16, k, off), int(b[k + 1] - b[k])) for k in range(N)]
+        base = torch.zeros(P + 8, dtype=torch.float16, device="cuda")
+        flat = base[off:off + P]
+        ss.ss_unshard(shards, b, flat)
+        assert torch.equal(flat.view(torch.int16), torch.cat([s.view(torch.int16) for s in shards]))
+        assert (base[:off] == 0).all() and (base[off + P:] == 0).all()
