@@ -261,3 +261,22 @@ def test_unshard_into_offset_flat(ss):
         ss.ss_unshard(shards, b, flat)
         assert torch.equal(flat.view(torch.int16), torch.cat([s.view(torch.int16) for s in shards]))
         assert (base[:off] == 0).all() and (base[off + P:] == 0).all()
+
+
+def test_step_paths_agree_and_no_timeouts(ss):
+    """The vector kernel (short calls) and the bulk-copy kernel (long calls) write identical bits."""
+    import torch
+    n, N, cut = 200_003, 8, 1000          # cut < one bulk tile: the first call takes the vector kernel
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 4) for r in range(N)]
+    G = [dev_bits(s, n) for s in specs]
+    a = _state(n)
+    b = _state(n)
+    pa = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    pb = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(HP, n, *a, rank_grads=G, param16=pa)
+    ss.ss_adam_step(HP, cut, *(t[:cut] for t in b), rank_grads=[g[:cut] for g in G], param16=pb[:cut])
+    ss.ss_adam_step(HP, n - cut, *(t[cut:] for t in b), rank_grads=[g[cut:] for g in G], param16=pb[cut:])
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+    assert ss.ss_device_error() == 0
