@@ -87,7 +87,6 @@ def _load():
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_last_cuda_error.restype = ctypes.c_char_p
     lib.ss_abi_version.restype = i32
-    lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     return lib
 
 
@@ -159,12 +158,6 @@ def _ptr_array(xs) -> ctypes.Array:
 def ss_abi_version() -> int:
     return int(_lib.ss_abi_version())
 
-
-def ss_device_error(clear: bool = False) -> int:
-    """The library's device error word on the current device (synchronises the device)."""
-    w = ctypes.c_uint32(0)
-    _check(_lib.ss_device_error(ctypes.byref(w), int(bool(clear))), "ss_device_error")
-    return int(w.value)
 
 
 def ss_flatten_layout(numels: Sequence[int], n_ranks: int):

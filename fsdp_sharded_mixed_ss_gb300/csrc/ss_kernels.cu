@@ -148,7 +148,6 @@ struct StepArgs {
   int64_t head;  // elements before the first 16-byte-aligned group (vector kernel only)
   int32_t n_ranks;
   float post_scale;
-  int32_t stages;  // bulk-copy pipeline depth (bulk kernel only)
   AdamConst k;
 };
 
@@ -421,284 +420,6 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
   }
 }
 
-// ------------------------------------------------------------------ fused AdamW step, bulk-copy pipeline
-//
-// Warp-specialised form of the fused step for large shards. One producer
-// thread streams tiles of the shard into shared memory with the Blackwell bulk
-// copy engine (cp.async.bulk, completion counted in bytes on an mbarrier);
-// CW consumer warps reduce the rank gradients, update the state and store the
-// results straight to global memory. Loads no longer wait behind the update
-// arithmetic: S slots of 16*T bytes keep ~190 KB per SM in flight while the
-// consumers work on the oldest slot.
-//
-// Tile: T = 256*CW elements. Consumer thread c owns elements 4c..4c+3 and
-// T/2+4c..T/2+4c+3 of a tile, so every shared-memory access of a warp is a
-// contiguous 256- or 512-byte run (no bank conflicts) and every global store
-// of a warp is a contiguous run as well. The tile's arrays -- each rank's
-// gradients (2 B/elem), then master, m, v (4 B/elem; or the fp32 gradient
-// first when the gradient is given in fp32) -- are packed greedily into
-// slots of 16*T bytes, in that fixed order, by producer and consumers alike.
-//
-// Every wait is bounded (about one second of %globaltimer); on expiry the
-// kernel records SS_DEVERR_TIMEOUT in the library's device error word and
-// returns instead of hanging.
-
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-enum : uint32_t { SS_DEVERR_TIMEOUT = 1u };
-
-__device__ uint32_t g_device_error = 0;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-
-// Wait for the phase of the given parity to complete, for at most ~1 s.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
-      atomicOr(&g_device_error, SS_DEVERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Global -> shared bulk copy; bytes and both addresses are multiples of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Arrays of a tile in order: ranks 0..N-1 (2 B/elem), then [g32,] master, m, v (4 B/elem).
-// Greedy packing into slots of 16*T bytes (in units of T/2 bytes: 4 per rank, 8 per fp32 array).
-__device__ __forceinline__ int item_end(int x, int n_arrays, int n_ranks) {
-  int units = 0;
-  int y = x;
-  while (y < n_arrays) {
-    const int u = y < n_ranks ? 4 : 8;
-    if (units + u > 32) break;
-    units += u;
-    ++y;
-  }
-  return y;
-}
-
-template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR, int CW>
-__global__ void __launch_bounds__((CW + 1) * 32, 1) adam_bulk_kernel(const __grid_constant__ StepArgs<MAXR> a) {
-  constexpr int T = 256 * CW;
-  constexpr int H = T / 2;
-  constexpr uint32_t SLOT = 16u * T;
-  extern __shared__ __align__(128) unsigned char smem[];
-  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
-  const int S = a.stages;
-  const uint32_t base = smem_addr(smem);
-  const uint32_t full0 = base + S * SLOT;         // S full barriers, then S empty barriers
-  const uint32_t empty0 = full0 + 8u * S;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8u * s, 1u);
-      mbar_init(empty0 + 8u * s, static_cast<uint32_t>(CW));
-    }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  __syncthreads();
-
-  const int n_ranks = FROM_G32 ? 0 : a.n_ranks;
-  const int n_arrays = FROM_G32 ? 4 : n_ranks + 3;
-  const int64_t nvec = (a.n - a.head) / kGroup;
-  const int64_t body = nvec * kGroup;
-  const int64_t ntiles = (body + T - 1) / T;
-
-  if (warp == CW) {
-    // ---------------- producer (one thread)
-    if (lane == 0) {
-      uint32_t it = 0;
-      bool ok = true;
-      for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-        const int64_t e = a.head + tile * T;
-        const uint32_t L = static_cast<uint32_t>(body - tile * T < T ? body - tile * T : T);
-        for (int x = 0; ok && x < n_arrays;) {
-          const int x2 = item_end(x, n_arrays, n_ranks);
-          const uint32_t slot = it % S, round = it / S;
-          if (!mbar_wait(empty0 + 8u * slot, (round & 1u) ^ 1u)) {
-            ok = false;
-            break;
-          }
-          uint32_t bytes = 0;
-          for (int y = x; y < x2; ++y) bytes += (y < n_ranks ? 2u : 4u) * L;
-          const uint32_t fb = full0 + 8u * slot;
-          mbar_expect_tx(fb, bytes);
-          uint32_t off = base + slot * SLOT;
-          for (int y = x; y < x2; ++y) {
-            const void* src;
-            uint32_t sz;
-            if (y < n_ranks) {
-              src = static_cast<const uint16_t*>(a.ranks.p[y]) + e;
-              sz = 2u * L;
-            } else {
-              const int z = y - n_ranks - (FROM_G32 ? 1 : 0);
-              const float* arr = z < 0 ? a.g32 : (z == 0 ? a.master : (z == 1 ? a.m : a.v));
-              src = arr + e;
-              sz = 4u * L;
-            }
-            bulk_load(off, src, sz, fb);
-            off += sz;
-          }
-          x = x2;
-          ++it;
-        }
-      }
-      // drain: every issued copy has landed before the block may exit
-      const uint32_t first = it > static_cast<uint32_t>(S) ? it - S : 0u;
-      for (uint32_t j = first; j < it; ++j) mbar_wait(full0 + 8u * (j % S), (j / S) & 1u);
-    }
-    return;
-  }
-
-  // ---------------- consumers
-  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
-  const int c = threadIdx.x;  // 0 .. 32*CW-1
-  bool bad = false;
-  uint32_t it = 0;
-  bool ok = true;
-  for (int64_t tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
-    const int64_t e = a.head + tile * T;
-    const int L = static_cast<int>(body - tile * T < T ? body - tile * T : T);
-    const bool v0 = 4 * c < L, v1 = H + 4 * c < L;
-    float g[8], p[8], m[8], v[8];
-    for (int x = 0; ok && x < n_arrays;) {
-      const int x2 = item_end(x, n_arrays, n_ranks);
-      const uint32_t slot = it % S, round = it / S;
-      ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8u * slot, round & 1u));   // warp-uniform outcome
-      if (!ok) break;
-      const unsigned char* sp = smem + slot * SLOT;
-      for (int y = x; y < x2; ++y) {
-        if (y < n_ranks) {
-          uint2 w0 = make_uint2(0u, 0u), w1 = make_uint2(0u, 0u);
-          if (v0) w0 = *reinterpret_cast<const uint2*>(sp + 8 * c);
-          if (v1) w1 = *reinterpret_cast<const uint2*>(sp + 2 * H + 8 * c);
-          const float2 f0 = widen2<GT>(w0.x), f1 = widen2<GT>(w0.y), f2 = widen2<GT>(w1.x), f3 = widen2<GT>(w1.y);
-          const float t8[8] = {f0.x, f0.y, f1.x, f1.y, f2.x, f2.y, f3.x, f3.y};
-          if (y == 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = t8[j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = g[j] + t8[j];
-          }
-          sp += 2 * L;
-        } else {
-          float4 q0 = make_float4(0.f, 0.f, 0.f, 0.f), q1 = q0;
-          if (v0) q0 = *reinterpret_cast<const float4*>(sp + 16 * c);
-          if (v1) q1 = *reinterpret_cast<const float4*>(sp + 4 * H + 16 * c);
-          const float t8[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-          const int z = y - n_ranks - (FROM_G32 ? 1 : 0);
-          if (z < 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = t8[j];
-          } else if (z == 0) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) p[j] = t8[j];
-          } else if (z == 1) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) m[j] = t8[j];
-          } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = t8[j];
-          }
-          sp += 4 * L;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8u * slot);
-      x = x2;
-      ++it;
-    }
-    if (!ok) break;
-    if constexpr (!FROM_G32) {
-      if (a.post_scale != 1.0f) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
-      }
-    }
-    if (a.nonfinite) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) bad |= (j < 4 ? v0 : v1) && !finite(g[j]);
-    }
-    const int64_t e0 = e + 4 * c, e1 = e + H + 4 * c;
-    if (a.g_out) {
-      if (v0) __stcs(reinterpret_cast<float4*>(a.g_out + e0), make_float4(g[0], g[1], g[2], g[3]));
-      if (v1) __stcs(reinterpret_cast<float4*>(a.g_out + e1), make_float4(g[4], g[5], g[6], g[7]));
-    }
-    if (a.dev_scale) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
-    }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
-    if (v0) {
-      __stcs(reinterpret_cast<float4*>(a.master + e0), make_float4(p[0], p[1], p[2], p[3]));
-      __stcs(reinterpret_cast<float4*>(a.m + e0), make_float4(m[0], m[1], m[2], m[3]));
-      __stcs(reinterpret_cast<float4*>(a.v + e0), make_float4(v[0], v[1], v[2], v[3]));
-      if constexpr (WRITE_P16)
-        __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.p16) + e0),
-               make_uint2(narrow2<PT>(p[0], p[1]), narrow2<PT>(p[2], p[3])));
-    }
-    if (v1) {
-      __stcs(reinterpret_cast<float4*>(a.master + e1), make_float4(p[4], p[5], p[6], p[7]));
-      __stcs(reinterpret_cast<float4*>(a.m + e1), make_float4(m[4], m[5], m[6], m[7]));
-      __stcs(reinterpret_cast<float4*>(a.v + e1), make_float4(v[4], v[5], v[6], v[7]));
-      if constexpr (WRITE_P16)
-        __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.p16) + e1),
-               make_uint2(narrow2<PT>(p[4], p[5]), narrow2<PT>(p[6], p[7])));
-    }
-  }
-  // the (< 8) elements before the aligned body and the (< 8) after it
-  if (blockIdx.x == 0) {
-    const int64_t tail0 = a.head + body;
-    if (c < a.head + (a.n - tail0)) step1<GT, PT, FROM_G32, WRITE_P16>(a, c < a.head ? c : tail0 + (c - a.head), gs, bad);
-  }
-  if (a.nonfinite) {
-    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
-    if (any && lane == 0) *a.nonfinite = 1;
-  }
-}
-
 // ------------------------------------------------------------------ host helpers
 
 struct Range {
@@ -772,28 +493,25 @@ ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream) {
 
 bool is16(ss_dtype d) { return d == SS_BF16 || d == SS_FP16; }
 
+// Splits a double into an fp32 pair hi + lo (hi = nearest float, lo = nearest float to the rest).
+void split(double x, float& hi, float& lo) {
+  hi = static_cast<float>(x);
+  lo = static_cast<float>(x - static_cast<double>(hi));
+}
+
 AdamConst make_const(const ss_adamw_hparams& hp) {
   const double b1 = hp.beta1, b2 = hp.beta2;
   const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp.step));
   const double bc2 = 1.0 - std::pow(b2, static_cast<double>(hp.step));
-  const double S = static_cast<double>(hp.lr) / bc1;
-  const double R = 1.0 / std::sqrt(bc2);
-  const double L = static_cast<double>(hp.lr) * static_cast<double>(hp.weight_decay);
-  const double c1 = 1.0 - b1, c2 = 1.0 - b2;
+  const double sq = std::sqrt(bc2);
   AdamConst k;
   k.b1 = hp.beta1;
-  k.c1 = static_cast<float>(c1);
-  k.c1_lo = static_cast<float>(c1 - static_cast<double>(k.c1));
+  split(1.0 - b1, k.c1, k.c1_lo);
   k.b2 = hp.beta2;
-  k.c2 = static_cast<float>(c2);
-  k.c2_lo = static_cast<float>(c2 - static_cast<double>(k.c2));
-  k.eps = hp.eps;
-  k.S_hi = static_cast<float>(S);
-  k.S_lo = static_cast<float>(S - static_cast<double>(k.S_hi));
-  k.R_hi = static_cast<float>(R);
-  k.R_lo = static_cast<float>(R - static_cast<double>(k.R_hi));
-  k.L_hi = static_cast<float>(L);
-  k.L_lo = static_cast<float>(L - static_cast<double>(k.L_hi));
+  split(1.0 - b2, k.c2, k.c2_lo);
+  split(static_cast<double>(hp.lr) * sq / bc1, k.A_hi, k.A_lo);
+  split(static_cast<double>(hp.eps) * sq, k.E_hi, k.E_lo);
+  split(1.0 - static_cast<double>(hp.lr) * static_cast<double>(hp.weight_decay), k.D_hi, k.D_lo);
   return k;
 }
 
@@ -807,57 +525,13 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 // ---- dispatch tables (template instantiation by runtime dtype / options)
 
-#ifndef SS_BULK_WARPS
-#define SS_BULK_WARPS 8
-#endif
-constexpr int kBulkWarps = SS_BULK_WARPS;     // consumer warps of the bulk-copy kernel
-constexpr int kBulkTile = 256 * kBulkWarps;   // elements per tile
-constexpr uint32_t kBulkSlot = 16u * kBulkTile;
-
-// Pipeline depth that fits the opt-in shared memory of the current device.
-int bulk_stages() {
-  int dev = 0, optin = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
-  return std::min(8, (optin - 256) / static_cast<int>(kBulkSlot + 16u));
-}
-
-// Raise a kernel's dynamic shared memory limit once (cached per kernel).
-bool allow_smem(const void* fn, size_t bytes) {
-  static std::mutex mu;
-  static std::vector<std::pair<const void*, size_t>> done;
-  std::lock_guard<std::mutex> lock(mu);
-  for (auto& d : done)
-    if (d.first == fn && d.second >= bytes) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
-    return false;
-  done.emplace_back(fn, bytes);
-  return true;
-}
-
-template <typename Args, typename Fn>
-ss_status launch_bulk(Fn* fn, Args a, void* stream) {
-  const int S = bulk_stages();
-  if (S < 2) return SS_ERR_CUDA;
-  a.stages = S;
-  const size_t smem = static_cast<size_t>(S) * (kBulkSlot + 16u);
-  if (!allow_smem(reinterpret_cast<const void*>(fn), smem)) return cuda_fail(cudaGetLastError());
-  const int64_t body = (a.n - a.head) / kGroup * kGroup;
-  const int64_t ntiles = (body + kBulkTile - 1) / kBulkTile;
-  const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(ntiles, sm_count())));
-  fn<<<grid, (kBulkWarps + 1) * 32, smem, static_cast<cudaStream_t>(stream)>>>(a);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SS_OK : cuda_fail(e);
-}
-
-enum class Path { kScalar, kVector, kBulk };
+enum class Path { kScalar, kVector };
 
 template <int MAXR>
 ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
                    void* stream) {
 #define SS_ADAM_CASE(G, P, F, W)                                                          \
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
-    if (path == Path::kBulk) return launch_bulk(adam_bulk_kernel<G, P, F, W, MAXR, kBulkWarps>, a, stream); \
     if (path == Path::kVector) {                                                          \
       auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                       \
       return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
@@ -937,18 +611,6 @@ using namespace ss;
 extern "C" {
 
 const char* ss_last_cuda_error(void) { return g_cuda_err; }
-
-ss_status ss_device_error(uint32_t* out, int32_t clear) {
-  if (!out) return SS_ERR_INVALID_ARG;
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(uint32_t));
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (clear) {
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  return SS_OK;
-}
 
 ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtype gdtype, int64_t n,
                          float post_scale, int32_t accumulate, float* g_out, int32_t* nonfinite_flag,
@@ -1042,7 +704,7 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
   if (n == 0) return SS_OK;
   const int h = common_phase(p16, p32);
   const bool vec = h >= 0 && h < n;
-  const Path path = !vec ? Path::kScalar : (n - h >= kBulkTile ? Path::kBulk : Path::kVector);
+  const Path path = vec ? Path::kVector : Path::kScalar;
   const AdamConst k = make_const(*hp);
   auto fill = [&](auto& a) {
     if (!from_g32)

@@ -69,20 +69,21 @@ SS_HD float approx_rcp(float x) {
 }
 
 // Step constants, prepared on the host in double and split into fp32 pairs.
+// With bc1 = 1 - beta1^t and bc2 = 1 - beta2^t the AdamW step
+//   p' = p (1 - lr wd) - (lr / bc1) m' / (sqrt(v' / bc2) + eps)
+// is evaluated as p' = p D - A m' / (sqrt(v') + E), multiplying numerator and
+// denominator by sqrt(bc2):  D = 1 - lr wd,  A = lr sqrt(bc2) / bc1,
+// E = eps sqrt(bc2).
 struct AdamConst {
   float b1, c1, c1_lo;  // beta1 ; 1 - beta1 as an fp32 pair (lo = 0 when beta1 >= 0.5)
   float b2, c2, c2_lo;  // beta2 ; 1 - beta2 as an fp32 pair
-  float eps;
-  float S_hi, S_lo;  // lr / (1 - beta1^t)
-  float R_hi, R_lo;  // 1 / sqrt(1 - beta2^t)
-  float L_hi, L_lo;  // lr * weight_decay
+  float A_hi, A_lo;
+  float E_hi, E_lo;
+  float D_hi, D_lo;
 };
 
 // One AdamW step of one element, in place:
-//   m' = b1 m + (1-b1) g ;  v' = b2 v + (1-b2) g^2
-//   p' = p - ( lr*wd * p + S * m' / (sqrt(v') * R + eps) )
-// which is p (1 - lr wd) - lr * mhat / (sqrt(vhat) + eps) with the bias
-// corrections folded into S and R.
+//   m' = b1 m + (1-b1) g ;  v' = b2 v + (1-b2) g^2 ;  p' = p D - A m' / (sqrt(v') + E)
 SS_HD void adamw_elem(const AdamConst& k, float g, float& p, float& m, float& v) {
   // first moment
   dd a = two_prod(k.b1, m);
@@ -105,28 +106,23 @@ SS_HD void adamw_elem(const AdamConst& k, float g, float& p, float& m, float& v)
     float res = fmaf(-r0, r0, vv.hi) + vv.lo;
     r = fast_two_sum(r0, res * (0.5f * rs));
   }
-  // d = r * R + eps
-  dd rr = two_prod(r.hi, k.R_hi);
-  rr.lo = fmaf(r.hi, k.R_lo, fmaf(r.lo, k.R_hi, rr.lo));
-  rr = fast_two_sum(rr.hi, rr.lo);
-  dd de = two_sum(rr.hi, k.eps);
-  dd d = fast_two_sum(de.hi, de.lo + rr.lo);
+  // d = r + E
+  dd de = two_sum(r.hi, k.E_hi);
+  dd d = fast_two_sum(de.hi, de.lo + (r.lo + k.E_lo));
   // u1 = m' / d: approximate quotient plus one remainder correction
   float rc = approx_rcp(d.hi);
   float q0 = mm.hi * rc;
   dd qd = two_prod(q0, d.hi);
   float rem = fmaf(-q0, d.lo, ((mm.hi - qd.hi) - qd.lo) + mm.lo);
   dd qq = fast_two_sum(q0, rem * rc);
-  // u = S * u1 + L * p
-  dd aa = two_prod(k.S_hi, qq.hi);
-  aa.lo = fmaf(k.S_hi, qq.lo, fmaf(k.S_lo, qq.hi, aa.lo));
-  dd w = two_prod(p, k.L_hi);
-  w.lo = fmaf(p, k.L_lo, w.lo);
-  dd u = two_sum(aa.hi, w.hi);
-  u.lo = u.lo + (aa.lo + w.lo);
-  // p' = p - u, rounded once
-  dd z = two_sum(p, -u.hi);
-  p = z.hi + (z.lo - u.lo);
+  // u = A * u1
+  dd u = two_prod(k.A_hi, qq.hi);
+  u.lo = fmaf(k.A_hi, qq.lo, fmaf(k.A_lo, qq.hi, u.lo));
+  // p' = p D - u, rounded once
+  dd pd = two_prod(p, k.D_hi);
+  pd.lo = fmaf(p, k.D_lo, pd.lo);
+  dd z = two_sum(pd.hi, -u.hi);
+  p = z.hi + (z.lo + (pd.lo - u.lo));
   m = mm.hi;
   v = vv.hi;
 }

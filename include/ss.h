@@ -189,13 +189,6 @@ ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ra
 /* ------------------------------------------------------------------- misc */
 const char* ss_status_string(ss_status s);      /* static string, never NULL */
 const char* ss_last_cuda_error(void);           /* last CUDA error text of this thread ("" if none) */
-
-/* The library's device error word on the current device: bit 0 (value 1) is
- * set by a kernel whose pipeline wait gave up after about one second (it then
- * returned early and its outputs are incomplete). Copies the word to *out
- * (host) and, when clear != 0, resets it. Synchronous: it waits for all work
- * queued on the device before reading. */
-ss_status ss_device_error(uint32_t* out, int32_t clear);
 int32_t ss_abi_version(void);                   /* SS_ABI_VERSION */
 
 #ifdef __cplusplus
