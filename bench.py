@@ -62,16 +62,19 @@ def measured_peaks() -> dict:
 
 
 def profile_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, if its source hash still matches."""
+    """DRAM bytes per launch from the committed ncu summary, while the kernel sources still match it."""
     import hashlib
 
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    path = os.path.join(ROOT, "profiles", "adam_traffic.txt")
     if not os.path.exists(path):
         return None
+    ent = {}
     with open(path) as f:
-        d = json.load(f)
-    ent = d.get(kernel)
-    if not ent:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                ent[k.strip()] = v.strip()
+    if ent.get("kernel") != kernel:
         return None
     src = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "csrc")
     h = hashlib.sha256()
@@ -80,7 +83,7 @@ def profile_traffic(kernel: str):
             h.update(f.read())
     if ent.get("csrc_sha256") != h.hexdigest():
         return None                     # the kernels changed since the counters were taken
-    return ent.get("dram_bytes_per_launch_full")
+    return int(ent["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -329,7 +332,7 @@ def cpu_baseline(target_s: float = 12.0) -> dict:
     sample = 1 << 21
     b, times, cores = oracle_sample_step(sample, 2)
     per = max(times[-1], 1e-6)
-    reps = max(3, min(200, int(target_s / per)))
+    reps = max(3, min(5000, int(target_s / per)))
     b, times, cores = oracle_sample_step(sample, reps)
     gbs = b * len(times) / sum(times) / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
