@@ -87,6 +87,10 @@ def _load():
     lib.ss_status_string.restype = ctypes.c_char_p
     lib.ss_last_cuda_error.restype = ctypes.c_char_p
     lib.ss_abi_version.restype = i32
+    lib.ss_grad_sumsq_workspace.argtypes = [i64]
+    lib.ss_grad_sumsq_workspace.restype = i64
+    lib.ss_grad_sumsq.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, i64, vp, vp, vp]
+    lib.ss_clip_coef.argtypes = [vp, i32, f32, vp, vp, vp]
     return lib
 
 
@@ -227,6 +231,35 @@ def ss_adam_step(hp: dict, n: int, master, m, v, *, g32=None, rank_grads=None, g
                                  len(ranks), -1 if gdtype is None else gdtype, float(post_scale), _ptr(master), _ptr(m),
                                  _ptr(v), _ptr(param16), -1 if pdtype is None else pdtype, ctypes.byref(opts),
                                  _stream(stream, master)), "ss_adam_step")
+
+
+def ss_grad_sumsq_workspace(n: int) -> int:
+    """Bytes of device workspace ss_grad_sumsq needs for a shard of n elements."""
+    return int(_lib.ss_grad_sumsq_workspace(n))
+
+
+def ss_grad_sumsq(n: int, sumsq_out, workspace, *, g32=None, rank_grads=None, gdtype: int | None = None,
+                  post_scale: float = 1.0, g_out=None, nonfinite_flag=None, workspace_bytes: int | None = None,
+                  stream=None) -> None:
+    """sumsq_out[0] (float64) = sum of squares of the shard's reduced gradient (workspace: device scratch)."""
+    ranks = rank_grads or []
+    if g32 is None and gdtype is None and ranks:
+        gdtype = _dtype_of(ranks[0])
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size()
+    ptrs = _ptr_array(ranks) if ranks else None
+    with _DeviceGuard(sumsq_out):
+        _check(_lib.ss_grad_sumsq(n, _ptr(g32), ctypes.cast(ptrs, ctypes.c_void_p) if ptrs else None, len(ranks),
+                                  -1 if gdtype is None else gdtype, float(post_scale), _ptr(sumsq_out),
+                                  _ptr(workspace), int(workspace_bytes), _ptr(g_out), _ptr(nonfinite_flag),
+                                  _stream(stream, sumsq_out)), "ss_grad_sumsq")
+
+
+def ss_clip_coef(shard_sumsq, n_shards: int, max_norm: float, coef_out, *, norm_out=None, stream=None) -> None:
+    """coef_out[0] = min(1, max_norm / (sqrt(sum of shard_sumsq[:n_shards]) + 1e-6))."""
+    with _DeviceGuard(coef_out):
+        _check(_lib.ss_clip_coef(_ptr(shard_sumsq), n_shards, float(max_norm), _ptr(coef_out), _ptr(norm_out),
+                                 _stream(stream, coef_out)), "ss_clip_coef")
 
 
 def ss_unshard(shards, shard_bounds: np.ndarray, flat, *, dtype: int | None = None, stream=None) -> None:

@@ -333,6 +333,148 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
   }
 }
 
+// ------------------------------------------------------------------ gradient sum of squares (global clip norm)
+//
+// Deterministic per-shard sum of squares of the reduced gradient. The shard is
+// cut into tiles of kThreads x 8 elements (after the 0..7-element head that
+// aligns the vectors); thread j of a tile owns its 8 consecutive elements and
+// adds their squares in fp32 (a fixed FMA chain), the block combines its
+// threads' sums in double through a fixed shuffle tree, and writes ONE double
+// per tile into the caller's workspace. The head/tail elements (< 16) get a
+// slot of their own. A second one-block kernel adds the slots in index order.
+// The partition depends only on n and the arrays' 16-byte phase, never on the
+// grid size, so the result is bit-reproducible.
+//
+// Error: each 8-element fp32 chain of non-negative terms is within 8 * 2^-24
+// relative of its exact value; the double sums add < 2^-40; so the result is
+// within ~5e-7 relative of the exact sum of squares of the fp32 gradients.
+
+template <int MAXR>
+struct SumsqArgs {
+  RankTable<MAXR> ranks;
+  const float* g32;
+  float* g_out;
+  int32_t* nonfinite;
+  double* partials;  // [ntiles + 1]
+  int64_t n;
+  int64_t head;
+  int64_t ntiles;
+  int32_t n_ranks;
+  float post_scale;
+};
+
+constexpr int kSumsqTile = kThreads * kGroup;
+
+__device__ __forceinline__ double block_sum(double x, double* red) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = x;
+  __syncthreads();
+  double s = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+  __syncthreads();
+  return s;  // meaningful in thread 0
+}
+
+template <int GT, bool FROM_G32, bool VEC, int MAXR>
+__device__ __forceinline__ float reduced1(const SumsqArgs<MAXR>& a, int64_t e) {
+  if constexpr (FROM_G32) return a.g32[e];
+  float g = reduce1<GT>(a.ranks, a.n_ranks, e);
+  if (a.post_scale != 1.0f) g = g * a.post_scale;
+  return g;
+}
+
+template <int GT, bool FROM_G32, bool VEC, int MAXR>
+__global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
+  __shared__ double red[kThreads / 32];
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  bool bad = false;
+  for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
+    const int64_t gi = tile * kThreads + threadIdx.x;
+    float s = 0.0f;
+    if (gi < nvec) {
+      const int64_t e = a.head + gi * kGroup;
+      float g[8];
+      if constexpr (VEC) {
+        if constexpr (FROM_G32) {
+          ld8f(a.g32 + e, g);
+        } else {
+          reduce8<GT>(a.ranks, a.n_ranks, e, g);
+          if (a.post_scale != 1.0f) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = reduced1<GT, FROM_G32, VEC>(a, e + j);
+      }
+      if (a.g_out) {
+        if constexpr (VEC) {
+          st8f(a.g_out + e, g);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        bad |= !finite(g[j]);
+        s = fmaf(g[j], g[j], s);
+      }
+    }
+    const double t = block_sum(static_cast<double>(s), red);
+    if (threadIdx.x == 0) a.partials[tile] = t;
+  }
+  // head and tail (< 16 elements) in slot ntiles, summed in element order by one thread
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const int64_t tail0 = a.head + nvec * kGroup;
+    double s = 0.0;
+    for (int64_t i = 0; i < a.head + (a.n - tail0); ++i) {
+      const int64_t e = i < a.head ? i : tail0 + (i - a.head);
+      const float g = reduced1<GT, FROM_G32, VEC>(a, e);
+      if (a.g_out) a.g_out[e] = g;
+      bad |= !finite(g);
+      s += static_cast<double>(fmaf(g, g, 0.0f));
+    }
+    a.partials[a.ntiles] = s;
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// out = sum of partials[0..count) in a fixed order (one block).
+__global__ void __launch_bounds__(1024) sum_slots_kernel(const double* partials, int64_t count, double* out) {
+  __shared__ double red[32];
+  double s = 0.0;
+  for (int64_t i = threadIdx.x; i < count; i += blockDim.x) s += partials[i];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+    *out = t;
+  }
+}
+
+// Global clip coefficient from the shards' sums of squares, added in rank order.
+__global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef,
+                                 double* norm_out) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double total = 0.0;
+  for (int32_t k = 0; k < n_shards; ++k) total += shard_sumsq[k];
+  const double norm = sqrt(total);
+  const double c = static_cast<double>(max_norm) / (norm + 1e-6);
+  *coef = static_cast<float>(c < 1.0 ? c : 1.0);
+  if (norm_out) *norm_out = norm;
+}
+
 // ------------------------------------------------------------------ unshard / reshard copies
 
 template <int MAXR>
@@ -606,6 +748,96 @@ ss_status check_ranks(const void* const* rank_grads, int32_t n_ranks, ss_dtype g
 }  // namespace
 }  // namespace ss
 
+namespace ss {
+namespace {
+
+template <int MAXR>
+ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
+  const unsigned grid = static_cast<unsigned>(
+      std::max<int64_t>(1, std::min<int64_t>(a.ntiles, static_cast<int64_t>(sm_count()) * 4)));
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+#define SS_SUMSQ_CASE(G, F, V)                                                   \
+  if (gt == G && from_g32 == F && vec == V) sumsq_tiles_kernel<G, F, V, MAXR><<<grid, kThreads, 0, st>>>(a);
+  SS_SUMSQ_CASE(SS_BF16, false, true)
+  else SS_SUMSQ_CASE(SS_BF16, false, false)
+  else SS_SUMSQ_CASE(SS_FP16, false, true)
+  else SS_SUMSQ_CASE(SS_FP16, false, false)
+  else SS_SUMSQ_CASE(SS_BF16, true, true)
+  else SS_SUMSQ_CASE(SS_BF16, true, false)
+  else return SS_ERR_DTYPE;
+#undef SS_SUMSQ_CASE
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  sum_slots_kernel<<<1, 1024, 0, st>>>(a.partials, a.ntiles + 1, out);
+  e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+// Shared by ss_grad_sumsq and any entry point that supplies its own slots.
+ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                          ss_dtype gdtype, float post_scale, double* sumsq_out, double* slots, int64_t slots_bytes,
+                          float* g_out, int32_t* nonfinite_flag, void* stream) {
+  if (n < 0 || !sumsq_out || !slots) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  if (slots_bytes < ss_grad_sumsq_workspace(n)) return SS_ERR_INVALID_ARG;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  const bool from_g32 = g32 != nullptr;
+  if (from_g32) {
+    if (reinterpret_cast<uintptr_t>(g32) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g32, 4 * n, false));
+    p32.push_back(reinterpret_cast<uintptr_t>(g32));
+  } else {
+    ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+    if (st != SS_OK) return st;
+  }
+  if ((reinterpret_cast<uintptr_t>(sumsq_out) & 7u) || (reinterpret_cast<uintptr_t>(slots) & 7u)) return SS_ERR_ALIGN;
+  ranges.push_back(rng(sumsq_out, 8, true));
+  ranges.push_back(rng(slots, ss_grad_sumsq_workspace(n), true));
+  if (g_out) {
+    if (reinterpret_cast<uintptr_t>(g_out) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g_out, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(g_out));
+  }
+  if (nonfinite_flag) {
+    if (reinterpret_cast<uintptr_t>(nonfinite_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(nonfinite_flag, 4, true));
+  }
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  const int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  const int64_t head = vec ? h : 0;
+  const int64_t nvec = (n - head) / kGroup;
+  const int64_t ntiles = (nvec + kThreads - 1) / kThreads;
+  auto fill = [&](auto& a) {
+    if (!from_g32)
+      for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.g32 = g32;
+    a.g_out = g_out;
+    a.nonfinite = nonfinite_flag;
+    a.partials = slots;
+    a.n = n;
+    a.head = head;
+    a.ntiles = ntiles;
+    a.n_ranks = from_g32 ? 0 : n_ranks;
+    a.post_scale = post_scale;
+  };
+  const ss_dtype gt = from_g32 ? SS_BF16 : gdtype;
+  if (from_g32 || n_ranks <= kSmallRanks) {
+    SumsqArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+  }
+  SumsqArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+}
+
+}  // namespace
+}  // namespace ss
+
 using namespace ss;
 
 extern "C" {
@@ -736,6 +968,33 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
   std::memset(&a, 0, sizeof a);
   fill(a);
   return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, stream);
+}
+
+int64_t ss_grad_sumsq_workspace(int64_t n) {
+  if (n < 0) return -1;
+  return static_cast<int64_t>(sizeof(double)) * ((n + kSumsqTile - 1) / kSumsqTile + 2);
+}
+
+ss_status ss_grad_sumsq(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                        ss_dtype gdtype, float post_scale, double* sumsq_out, void* workspace,
+                        int64_t workspace_bytes, float* g_out, int32_t* nonfinite_flag, void* stream) {
+  return grad_sumsq_impl(n, g32, rank_grads, n_ranks, gdtype, post_scale, sumsq_out,
+                         static_cast<double*>(workspace), workspace_bytes, g_out, nonfinite_flag, stream);
+}
+
+ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef_out,
+                       double* norm_out, void* stream) {
+  if (!shard_sumsq || !coef_out || n_shards < 1 || !(max_norm > 0.0f) || !std::isfinite(max_norm))
+    return SS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(shard_sumsq) & 7u) || (reinterpret_cast<uintptr_t>(coef_out) & 3u) ||
+      (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u)))
+    return SS_ERR_ALIGN;
+  std::vector<Range> ranges = {rng(shard_sumsq, 8 * static_cast<int64_t>(n_shards), false), rng(coef_out, 4, true)};
+  if (norm_out) ranges.push_back(rng(norm_out, 8, true));
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  clip_coef_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(shard_sumsq, n_shards, max_norm, coef_out, norm_out);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
 }
 
 static ss_status copy_common(const void* const* src, void* const* dst, const int64_t* shard_bounds, int32_t n_ranks,

@@ -164,11 +164,41 @@ ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtyp
  * opts (host, optional): see ss_step_options.
  * Outputs (master, m, v, param16, g_out) must not overlap each other or the
  * inputs (SS_ERR_OVERLAP). With non-finite gradients the state becomes
- * non-finite; use nonfinite_flag in a prior ss_grad_reduce pass
+ * non-finite; use nonfinite_flag in a prior ss_grad_reduce or ss_grad_sumsq pass
  * with dev_skip_flag to skip such a step. */
 ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, const void* const* rank_grads,
                        int32_t n_ranks, ss_dtype gdtype, float post_scale, float* master, float* m, float* v,
                        void* param16, ss_dtype pdtype, const ss_step_options* opts, void* stream);
+
+/* ------------------------------------------------------- global clip norm
+ * "FSDP: Fully Sharded Data Parallel Training at Scale", gradient clipping:
+ * the clip norm is the norm of the whole gradient, so every shard contributes
+ * its sum of squares and the contributions are added across shards before the
+ * square root (a per-shard norm would underestimate it).
+ *
+ * ss_grad_sumsq: *sumsq_out (device double) = sum of g[i]^2 over the shard,
+ *   where g is the reduced gradient exactly as in ss_adam_step (rank-ordered
+ *   fp32 sum of rank_grads times post_scale, or g32). Optionally writes g to
+ *   g_out [n] fp32 and sets *nonfinite_flag to 1 when any g is inf/NaN.
+ *   workspace: device scratch of at least ss_grad_sumsq_workspace(n) bytes,
+ *   8-byte aligned, owned by the caller, overwritten (no initial contents
+ *   needed). Each group of 8 squares is added in fp32, the rest in double, in
+ *   an order fixed by n and the arrays' alignment (not by the launch), so the
+ *   result is reproducible and within 5e-7 relative of the exact sum.
+ *   Two kernel launches on `stream`.
+ * ss_grad_sumsq_workspace: the workspace size in bytes for a shard of n
+ *   elements (-1 if n < 0).
+ * ss_clip_coef: shard_sumsq [n_shards] (device doubles, one per shard) ->
+ *   norm = sqrt(sum in shard order), *coef_out (device float) =
+ *   min(1, max_norm / (norm + 1e-6)), the coefficient of the clip_grad_norm_
+ *   convention; *norm_out (device double, optional) = norm. Feed coef_out to
+ *   ss_adam_step as opts->dev_grad_scale. max_norm > 0 and finite. */
+int64_t ss_grad_sumsq_workspace(int64_t n);
+ss_status ss_grad_sumsq(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                        ss_dtype gdtype, float post_scale, double* sumsq_out, void* workspace,
+                        int64_t workspace_bytes, float* g_out, int32_t* nonfinite_flag, void* stream);
+ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef_out,
+                       double* norm_out, void* stream);
 
 /* ----------------------------------------------------------------- unshard
  * "FSDP: Fully Sharded Data Parallel Training at Scale", the unit's

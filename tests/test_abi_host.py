@@ -132,3 +132,25 @@ def test_reduce_and_copy_argument_errors(ss):
     with pytest.raises(ss.SSError) as e:
         ss.ss_reshard(0x70000000, b, [A, B, C, D], dtype=7, stream=0)
     assert e.value.status == 4
+
+
+def test_sumsq_and_clip_argument_errors(ss):
+    n = 10_000
+    ws = ss.ss_grad_sumsq_workspace(n)
+    assert ws == 8 * ((n + 2047) // 2048 + 2) and ss.ss_grad_sumsq_workspace(-1) == -1
+    W, O = 0x70000000, 0x71000000
+    with pytest.raises(ss.SSError) as e:            # workspace too small
+        ss.ss_grad_sumsq(n, O, W, rank_grads=[A, B], gdtype=ss.SS_BF16, workspace_bytes=ws - 8, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(ss.SSError) as e:            # output inside the workspace
+        ss.ss_grad_sumsq(n, W + 8, W, rank_grads=[A, B], gdtype=ss.SS_BF16, workspace_bytes=ws, stream=0)
+    assert e.value.status == 3
+    with pytest.raises(ss.SSError) as e:            # misaligned double output
+        ss.ss_grad_sumsq(n, O + 4, W, rank_grads=[A, B], gdtype=ss.SS_BF16, workspace_bytes=ws, stream=0)
+    assert e.value.status == 2
+    with pytest.raises(ss.SSError) as e:
+        ss.ss_clip_coef(O, 4, 0.0, O + 64, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(ss.SSError) as e:
+        ss.ss_clip_coef(O, 4, 1.0, O + 8, stream=0)  # coefficient overlaps the shard sums
+    assert e.value.status == 3
