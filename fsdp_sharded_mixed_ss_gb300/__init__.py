@@ -91,6 +91,7 @@ def _load():
     lib.ss_grad_sumsq_workspace.restype = i64
     lib.ss_grad_sumsq.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, i64, vp, vp, vp]
     lib.ss_clip_coef.argtypes = [vp, i32, f32, vp, vp, vp]
+    lib.ss_grad_sumsq_noalloc.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, vp, vp]
     return lib
 
 
@@ -253,6 +254,27 @@ def ss_grad_sumsq(n: int, sumsq_out, workspace, *, g32=None, rank_grads=None, gd
                                   -1 if gdtype is None else gdtype, float(post_scale), _ptr(sumsq_out),
                                   _ptr(workspace), int(workspace_bytes), _ptr(g_out), _ptr(nonfinite_flag),
                                   _stream(stream, sumsq_out)), "ss_grad_sumsq")
+
+
+SS_NOALLOC_SUMSQ_MAX_N = (65536 - 2) * 2048
+
+
+def ss_grad_sumsq_noalloc(n: int, sumsq_out, *, g32=None, rank_grads=None, gdtype: int | None = None,
+                          post_scale: float = 1.0, g_out=None, nonfinite_flag=None, stream=None) -> None:
+    """ss_grad_sumsq without a workspace argument: for callers that cannot allocate device memory.
+
+    The scratch lives in a fixed 512 KiB array inside the library, so n is limited to
+    SS_NOALLOC_SUMSQ_MAX_N and calls that may run concurrently on the GPU must not be issued.
+    """
+    ranks = rank_grads or []
+    if g32 is None and gdtype is None and ranks:
+        gdtype = _dtype_of(ranks[0])
+    ptrs = _ptr_array(ranks) if ranks else None
+    with _DeviceGuard(sumsq_out):
+        _check(_lib.ss_grad_sumsq_noalloc(n, _ptr(g32), ctypes.cast(ptrs, ctypes.c_void_p) if ptrs else None,
+                                          len(ranks), -1 if gdtype is None else gdtype, float(post_scale),
+                                          _ptr(sumsq_out), _ptr(g_out), _ptr(nonfinite_flag),
+                                          _stream(stream, sumsq_out)), "ss_grad_sumsq_noalloc")
 
 
 def ss_clip_coef(shard_sumsq, n_shards: int, max_norm: float, coef_out, *, norm_out=None, stream=None) -> None:

@@ -982,6 +982,59 @@ ss_status ss_grad_sumsq(int64_t n, const float* g32, const void* const* rank_gra
                          static_cast<double*>(workspace), workspace_bytes, g_out, nonfinite_flag, stream);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- sum of squares without allocation
+//
+// ss_grad_sumsq_noalloc keeps its tile slots in this fixed array instead of a
+// caller workspace, for callers that cannot allocate device memory. Every GPU
+// that loads the library holds the array (SS_NOALLOC_SUMSQ_SLOTS doubles =
+// 512 KiB) until the process exits. All calls share it: each call overwrites
+// every slot it reads before reading it, so nothing needs clearing, but two
+// calls whose kernels overlap on the GPU race on the slots.
+static __device__ __align__(256) double g_noalloc_sumsq_slots[SS_NOALLOC_SUMSQ_SLOTS];
+
+namespace {
+
+// Device address of the slot array on the current device. The name of the
+// array is only a host-side stand-in; the address comes from the runtime, once
+// per device, with that device current.
+ss_status noalloc_slots(double** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static double* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_sumsq_slots);
+    if (e != cudaSuccess) return cuda_fail(e);
+    addr[dev] = static_cast<double*>(p);
+  }
+  *out = addr[dev];
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                                ss_dtype gdtype, float post_scale, double* sumsq_out, float* g_out,
+                                int32_t* nonfinite_flag, void* stream) {
+  if (n < 0) return SS_ERR_INVALID_ARG;
+  if (n > SS_NOALLOC_SUMSQ_MAX_N) return SS_ERR_OVERFLOW;
+  double* slots = nullptr;
+  const ss_status st = noalloc_slots(&slots);
+  if (st != SS_OK) return st;
+  return grad_sumsq_impl(n, g32, rank_grads, n_ranks, gdtype, post_scale, sumsq_out, slots,
+                         static_cast<int64_t>(sizeof(double)) * SS_NOALLOC_SUMSQ_SLOTS, g_out, nonfinite_flag,
+                         stream);
+}
+
 ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef_out,
                        double* norm_out, void* stream) {
   if (!shard_sumsq || !coef_out || n_shards < 1 || !(max_norm > 0.0f) || !std::isfinite(max_norm))

@@ -200,6 +200,34 @@ ss_status ss_grad_sumsq(int64_t n, const float* g32, const void* const* rank_gra
 ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef_out,
                        double* norm_out, void* stream);
 
+/* ------------------------------------------ sum of squares without allocation
+ * No counterpart on the pages: an addition for callers that cannot allocate
+ * device memory -- for instance plugin code running inside another framework
+ * that has already reserved the GPU's memory for its own pool, or a
+ * latency-critical loop where cudaMalloc's implicit device synchronisation is
+ * not acceptable -- and so cannot provide ss_grad_sumsq's workspace.
+ *
+ * ss_grad_sumsq_noalloc computes exactly what ss_grad_sumsq computes (same
+ * kernels, same bits) but keeps its scratch in a fixed array inside the
+ * library: SS_NOALLOC_SUMSQ_SLOTS doubles (512 KiB), held on every GPU that
+ * loads the library until the process exits. It allocates nothing and frees
+ * nothing. The caller still passes the inputs and outputs, as for
+ * ss_grad_sumsq.
+ *   - n may be at most SS_NOALLOC_SUMSQ_MAX_N (134,213,632 elements);
+ *     larger n returns SS_ERR_OVERFLOW and launches nothing.
+ *   - The first call on a device looks up the array's device address with
+ *     the runtime (no allocation); make that first call before any stream
+ *     capture on that device.
+ *   - All calls share the one array: calls whose kernels may overlap on the
+ *     GPU (different streams without ordering) race and give wrong results.
+ *     Calls ordered on one stream are safe; nothing has to be cleared between
+ *     them. */
+#define SS_NOALLOC_SUMSQ_SLOTS 65536
+#define SS_NOALLOC_SUMSQ_MAX_N ((int64_t)(SS_NOALLOC_SUMSQ_SLOTS - 2) * 2048)
+ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                                ss_dtype gdtype, float post_scale, double* sumsq_out, float* g_out,
+                                int32_t* nonfinite_flag, void* stream);
+
 /* ----------------------------------------------------------------- unshard
  * "FSDP: Fully Sharded Data Parallel Training at Scale", the unit's
  * communication cycle (forward and backward all-gather): the full flat unit is

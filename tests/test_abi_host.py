@@ -154,3 +154,11 @@ def test_sumsq_and_clip_argument_errors(ss):
     with pytest.raises(ss.SSError) as e:
         ss.ss_clip_coef(O, 4, 1.0, O + 8, stream=0)  # coefficient overlaps the shard sums
     assert e.value.status == 3
+
+
+def test_noalloc_size_limit_rejected_on_host(ss):
+    # n above the fixed scratch capacity is refused before anything touches a GPU
+    with pytest.raises(ss.SSError) as e:
+        ss.ss_grad_sumsq_noalloc(ss.SS_NOALLOC_SUMSQ_MAX_N + 1, 0x70000000, g32=0x71000000, stream=0)
+    assert e.value.status == 5
+    assert ss.SS_NOALLOC_SUMSQ_MAX_N == (65536 - 2) * 2048
