@@ -186,6 +186,99 @@ def bytes_per_step(s) -> tuple[int, int]:
     return adam, unshard
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of per-rank timings over the process group (the job is as slow as its
+    slowest rank); identity without a group. Host bookkeeping only, not the data path."""
+    import torch
+    import torch.distributed as dist
+
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return list(values)
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank moves its own unit's bytes each step (weak scaling)."""
+    return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
+
+
+def run_e2e(s, steps: int, device, t_counter):
+    """Steps through the public API with the gradients copied in from pinned host memory and the
+    flat bf16 unit copied back, every step. Three streams: the host-to-device copy of step i+1 and
+    the device-to-host copy of step i-1 overlap step i (double-buffered device inputs and outputs).
+    Returns (ms per step, H2D GB/s alone, D2H GB/s alone)."""
+    import torch
+
+    ss, w = s["ss"], s["w"]
+    n, N, P = s["n"], s["N"], s["P"]
+    host_in = torch.empty((N, n), dtype=torch.bfloat16, pin_memory=True)
+    for r in range(N):
+        host_in[r].copy_(s["views"][r])
+    host_out = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+    dev_in = [torch.empty((N, n), dtype=torch.bfloat16, device=device) for _ in range(2)]
+    flat = [s["flat"], torch.empty(P, dtype=torch.bfloat16, device=device)]
+    s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(3))
+    done = {"h2d": {}, "cmp": {}, "d2h": {}}
+
+    def mark(kind, i, st):
+        e = torch.cuda.Event()
+        e.record(st)
+        done[kind][i] = e
+
+    def step(i):
+        b = i % 2
+        t = t_counter[0]
+        t_counter[0] += 1
+        if i - 2 in done["cmp"]:
+            s_h2d.wait_event(done["cmp"][i - 2])          # dev_in[b] no longer read
+        with torch.cuda.stream(s_h2d):
+            dev_in[b].copy_(host_in, non_blocking=True)
+        mark("h2d", i, s_h2d)
+        s_cmp.wait_event(done["h2d"][i])
+        if i - 2 in done["d2h"]:
+            s_cmp.wait_event(done["d2h"][i - 2])          # flat[b] already copied out
+        ss.ss_adam_step(w.hp(t), n, s["master"], s["m"], s["v"], rank_grads=[dev_in[b][r] for r in range(N)],
+                        param16=s["shards"][0], stream=s_cmp)
+        ss.ss_unshard(s["shards"], s["bounds"], flat[b], stream=s_cmp)
+        mark("cmp", i, s_cmp)
+        s_d2h.wait_event(done["cmp"][i])
+        with torch.cuda.stream(s_d2h):
+            host_out[b].copy_(flat[b], non_blocking=True)
+        mark("d2h", i, s_d2h)
+
+    for i in range(3):
+        step(i)
+    torch.cuda.synchronize(device)
+    for d in done.values():
+        d.clear()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_h2d)
+    for i in range(steps):
+        step(i)
+    s_d2h.wait_stream(s_h2d)
+    s_d2h.wait_stream(s_cmp)
+    e1.record(s_d2h)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1) / steps
+
+    # each copy direction alone, for reference
+    def timed(fn):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st = torch.cuda.current_stream(device)
+        a.record(st)
+        for _ in range(5):
+            fn()
+        b.record(st)
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / 5
+
+    h2d_ms = timed(lambda: dev_in[0].copy_(host_in, non_blocking=True))
+    d2h_ms = timed(lambda: host_out[0].copy_(flat[0], non_blocking=True))
+    return e2e_ms, 2 * N * n / (h2d_ms * 1e-3) / 1e9, 2 * P / (d2h_ms * 1e-3) / 1e9
+
+
 def run_ours(args, rank: int, world: int, device):
     import torch
     import torch.distributed as dist
@@ -233,42 +326,13 @@ def run_ours(args, rank: int, world: int, device):
     clocks = sampler.summary(h0, h1)
 
     # end to end through the public API with host buffers: pinned grads in, flat params out
-    n, N = s["n"], s["N"]
-    host_grads = [torch.empty(n, dtype=torch.bfloat16, pin_memory=True) for _ in range(N)]
-    for r in range(N):
-        host_grads[r].copy_(s["views"][r])
-    host_flat = torch.empty(s["P"], dtype=torch.bfloat16, pin_memory=True)
-    dev_in = [torch.empty(n, dtype=torch.bfloat16, device=device) for _ in range(N)]
-
-    def e2e_step():
-        t = t_counter[0]
-        t_counter[0] += 1
-        for r in range(N):
-            dev_in[r].copy_(host_grads[r], non_blocking=True)
-        ss.ss_adam_step(w.hp(t), n, s["master"], s["m"], s["v"], rank_grads=dev_in, param16=s["shards"][0],
-                        stream=stream)
-        ss.ss_unshard(s["shards"], s["bounds"], s["flat"], stream=stream)
-        host_flat.copy_(s["flat"], non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    torch.cuda.synchronize(device)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_ms, h2d_gbs, d2h_gbs = run_e2e(s, args.e2e_steps, device, t_counter)
 
     adam_b, unshard_b = bytes_per_step(s)
-    if world > 1:
-        t = torch.tensor([elapsed_ms, e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms, e2e_ms = t.tolist()
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], device if world > 1 else None)
     ms_per_step = elapsed_ms / args.steps
     total_bytes = (adam_b + unshard_b) * world
-    value = total_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_gbs(adam_b + unshard_b, world, ms_per_step)
     peaks = measured_peaks()
     achieved = adam_b / (adam_ms * 1e-3) / 1e9
     traffic = profile_traffic("adam_vec_kernel")
@@ -276,11 +340,11 @@ def run_ours(args, rank: int, world: int, device):
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "unit_params": s["P"], "virtual_ranks": N, "shard_elems": n,
+        "config": {"workload": WORKLOAD, "unit_params": s["P"], "virtual_ranks": s["N"], "shard_elems": s["n"],
                    "grad_dtype": "bf16", "param_dtype": "bf16", "state_dtype": "f32",
                    "bytes_per_step": adam_b + unshard_b,
                    "l2": "inputs larger than L2 (1.15 GB moved per step vs 129 MB L2); no flush"},
-        "params_per_s": round(n * world / (ms_per_step * 1e-3), 1),
+        "params_per_s": round(s["n"] * world / (ms_per_step * 1e-3), 1),
         "unit_params_per_s": round(s["P"] * world / (ms_per_step * 1e-3), 1),
         "roofline": {"kernel": "adam_vec_kernel (fused reduce + AdamW + bf16 cast)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -288,7 +352,9 @@ def run_ours(args, rank: int, world: int, device):
                      "algorithmic_bytes": adam_b, "avg_launch_ms": round(adam_ms, 5),
                      "peak_source": peaks["source"]},
         "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * n * N, "d2h_bytes_per_step": 2 * s["P"]},
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * s["n"] * s["N"],
+                "d2h_bytes_per_step": 2 * s["P"], "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
+                "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)"},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }

@@ -43,6 +43,15 @@ namespace ss {
 namespace {
 
 constexpr int kThreads = 256;
+// Block shape of the fused step kernel (the register-heavy one): threads per
+// block and the minimum resident blocks per SM asked of the compiler.
+#ifndef SS_STEP_THREADS
+#define SS_STEP_THREADS 256
+#endif
+#ifndef SS_STEP_MIN_BLOCKS
+#define SS_STEP_MIN_BLOCKS 1
+#endif
+constexpr int kStepThreads = SS_STEP_THREADS;
 constexpr int kGroup = 8;         // elements per thread per iteration
 constexpr int kSmallRanks = 64;   // pointer table size of the common kernels
 constexpr int kLargeRanks = SS_MAX_RANKS;
@@ -211,7 +220,7 @@ __device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float 
 }
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
-__global__ void __launch_bounds__(kThreads) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+__global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
@@ -607,28 +616,28 @@ int sm_count() {
   return sms;
 }
 
-// Resident blocks per SM of a kernel (cached per kernel).
-int blocks_per_sm(const void* fn) {
+// Resident blocks per SM of a kernel launched with `threads` per block (cached per kernel).
+int blocks_per_sm(const void* fn, int threads = kThreads) {
   static std::mutex mu;
   static std::vector<std::pair<const void*, int>> cache;
   std::lock_guard<std::mutex> lock(mu);
   for (auto& c : cache)
     if (c.first == fn) return c.second;
   int b = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, 0) != cudaSuccess || b < 1) b = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, 0) != cudaSuccess || b < 1) b = 1;
   cache.emplace_back(fn, b);
   return b;
 }
 
-unsigned grid_for(const void* fn, int64_t work_items) {
-  const int64_t want = std::max<int64_t>(1, (work_items + kThreads - 1) / kThreads);
-  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(fn));
+unsigned grid_for(const void* fn, int64_t work_items, int threads = kThreads) {
+  const int64_t want = std::max<int64_t>(1, (work_items + threads - 1) / threads);
+  const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(fn, threads));
   return static_cast<unsigned>(std::min(want, cap));
 }
 
 template <typename Args, typename Fn>
-ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream) {
-  fn<<<grid, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(args);
+ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream, int threads = kThreads) {
+  fn<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(args);
   cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? SS_OK : cuda_fail(e);
 }
@@ -676,7 +685,8 @@ ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, 
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
     if (path == Path::kVector) {                                                          \
       auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                       \
-      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
+      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kStepThreads), a, \
+                    stream, kStepThreads);                                                \
     }                                                                                     \
     auto* fn = adam_scalar_kernel<G, P, F, W, MAXR>;                                      \
     return launch(fn, grid_for(reinterpret_cast<const void*>(fn), a.n), a, stream);       \
