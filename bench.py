@@ -47,6 +47,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="instead of the benchmark line, time every kernel on the sweep and layer shapes")
+    ap.add_argument("--suite-n", type=int, default=1 << 26, help="shard length of the --suite runs")
     return ap.parse_args()
 
 
@@ -335,7 +338,7 @@ def run_ours(args, rank: int, world: int, device):
     value = job_gbs(adam_b + unshard_b, world, ms_per_step)
     peaks = measured_peaks()
     achieved = adam_b / (adam_ms * 1e-3) / 1e9
-    traffic = profile_traffic("adam_vec_kernel")
+    traffic = profile_traffic("adam_pipe_kernel")
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
@@ -346,7 +349,7 @@ def run_ours(args, rank: int, world: int, device):
                    "l2": "inputs larger than L2 (1.15 GB moved per step vs 129 MB L2); no flush"},
         "params_per_s": round(s["n"] * world / (ms_per_step * 1e-3), 1),
         "unit_params_per_s": round(s["P"] * world / (ms_per_step * 1e-3), 1),
-        "roofline": {"kernel": "adam_vec_kernel (fused reduce + AdamW + bf16 cast)", "bound": "hbm",
+        "roofline": {"kernel": "adam_pipe_kernel (fused reduce + AdamW + bf16 cast, N=8)", "bound": "hbm",
                      "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
                      "algorithmic_bytes": adam_b, "avg_launch_ms": round(adam_ms, 5),
@@ -359,6 +362,74 @@ def run_ours(args, rank: int, world: int, device):
         "clocks": clocks,
     }
     return result
+
+
+# ----------------------------------------------------------------------------- kernel suite
+
+def run_suite(args, device) -> dict:
+    """Mean CUDA-event time and algorithmic GB/s of each kernel on synthetic shards."""
+    import torch
+
+    import fsdp_sharded_mixed_ss_gb300 as ss
+    import synth
+
+    def timed(fn, reps=30):
+        # back-to-back launches between two events: the host stays ahead of the GPU, so
+        # the time is the kernels' own, not the host's launch latency
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(device)
+        return a.elapsed_time(b) / reps
+
+    def entry(ms, nbytes):
+        return {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
+
+    out = {"peak_hbm_gbs": measured_peaks()["hbm_gbs"], "n": args.suite_n}
+    n = args.suite_n
+    hp = dict(lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1000)
+    st = []
+    for spec in (synth.normal(0.02, synth.FP32, synth.MASTER), synth.normal(1e-4, synth.FP32, synth.MOM1),
+                 synth.normal(1e-8, synth.FP32, synth.MOM2, absolute=True)):
+        t = torch.empty(n, dtype=torch.float32, device=device)
+        synth.device_fill(spec, t.view(torch.int32))
+        st.append(t)
+    p16 = torch.empty(n, dtype=torch.bfloat16, device=device)
+    g32 = torch.empty(n, dtype=torch.float32, device=device)
+    synth.device_fill(synth.normal(1e-3, synth.FP32, synth.GRAD, 0, 1), g32.view(torch.int32))
+    out["adam_step_fp32_grad"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, g32=g32, param16=p16)), 30 * n)
+    ws = torch.empty(max(ss.ss_grad_sumsq_workspace(n) // 8, 1), dtype=torch.float64, device=device)
+    acc = torch.empty(1, dtype=torch.float64, device=device)
+    for N in (2, 8, 64):
+        G = []
+        for r in range(N):
+            t = torch.empty(n, dtype=torch.bfloat16, device=device)
+            synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+            G.append(t)
+        out[f"adam_step_N{N}"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=p16)),
+                                       (2 * N + 26) * n)
+        out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
+        out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
+        del G
+        torch.cuda.empty_cache()
+    del st, p16, g32, ws
+    torch.cuda.empty_cache()
+    for name, numels, N, dt in (("unshard_gpt2_small_N8", [124_439_808], 8, torch.bfloat16),
+                                ("unshard_llama70b_layer_N64", [855_654_400], 64, torch.float16)):
+        _, b = ss.ss_flatten_layout(numels, N)
+        P = int(b[-1])
+        shards = [torch.zeros(int(b[k + 1] - b[k]), dtype=dt, device=device) for k in range(N)]
+        flat = torch.empty(P, dtype=dt, device=device)
+        out[name] = entry(timed(lambda: ss.ss_unshard(shards, b, flat)), 4 * P)
+        out[name.replace("unshard", "reshard")] = entry(timed(lambda: ss.ss_reshard(flat, b, shards)), 4 * P)
+        del shards, flat
+        torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -443,6 +514,9 @@ def main():
         raise SystemExit("bench.py needs a CUDA GPU")
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
+    if args.suite:
+        print(json.dumps({"suite": run_suite(args, device)}), flush=True)
+        return
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
     result = run_ours(args, rank, world, device)

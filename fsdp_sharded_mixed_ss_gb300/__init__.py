@@ -256,7 +256,7 @@ def ss_grad_sumsq(n: int, sumsq_out, workspace, *, g32=None, rank_grads=None, gd
                                   _stream(stream, sumsq_out)), "ss_grad_sumsq")
 
 
-SS_NOALLOC_SUMSQ_MAX_N = (65536 - 2) * 2048
+SS_NOALLOC_SUMSQ_MAX_N = (65536 - 2) * 16384
 
 
 def ss_grad_sumsq_noalloc(n: int, sumsq_out, *, g32=None, rank_grads=None, gdtype: int | None = None,

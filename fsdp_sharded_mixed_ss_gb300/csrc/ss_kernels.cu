@@ -271,6 +271,99 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
   }
 }
 
+// Register double-buffered form for small rank counts: the loads of a
+// thread's next group are issued before the update of its current group, so
+// each thread keeps two groups of bytes in flight (for N <= SS_PIPE_MAX_RANKS,
+// where one group alone is too few bytes to cover HBM latency at the
+// residency the update's registers allow). NR is the rank count; with F the
+// gradient is the fp32 array g32, held as NR = 2 raw 16-byte chunks.
+#ifndef SS_PIPE_MAX_RANKS
+#define SS_PIPE_MAX_RANKS 8
+#endif
+template <int NR>
+struct PipeGroup {
+  uint4 r[NR];
+  float4 s[6];  // master, m, v: two float4 each
+};
+
+template <int GT, int NR, bool F, int MAXR>
+__device__ __forceinline__ void pipe_load(const StepArgs<MAXR>& a, int64_t gi, PipeGroup<NR>& G) {
+  const int64_t e = a.head + gi * kGroup;
+  if constexpr (F) {
+    static_assert(NR == 2, "the fp32 gradient occupies two chunks");
+    G.r[0] = __ldcs(reinterpret_cast<const uint4*>(a.g32 + e));
+    G.r[1] = __ldcs(reinterpret_cast<const uint4*>(a.g32 + e) + 1);
+  } else {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) G.r[r] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e));
+  }
+  G.s[0] = __ldcs(reinterpret_cast<const float4*>(a.master + e));
+  G.s[1] = __ldcs(reinterpret_cast<const float4*>(a.master + e) + 1);
+  G.s[2] = __ldcs(reinterpret_cast<const float4*>(a.m + e));
+  G.s[3] = __ldcs(reinterpret_cast<const float4*>(a.m + e) + 1);
+  G.s[4] = __ldcs(reinterpret_cast<const float4*>(a.v + e));
+  G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + e) + 1);
+}
+
+template <int GT, int PT, bool F, bool WRITE_P16, int MAXR, int NR>
+__global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  PipeGroup<NR> cur, nxt;
+  if (tid < nvec) pipe_load<GT, NR, F>(a, tid, cur);
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    if (gi + stride < nvec) pipe_load<GT, NR, F>(a, gi + stride, nxt);
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (F) {
+      const uint4 x = cur.r[0], y = cur.r[1];
+      g[0] = __uint_as_float(x.x); g[1] = __uint_as_float(x.y); g[2] = __uint_as_float(x.z); g[3] = __uint_as_float(x.w);
+      g[4] = __uint_as_float(y.x); g[5] = __uint_as_float(y.y); g[6] = __uint_as_float(y.z); g[7] = __uint_as_float(y.w);
+    } else {
+      widen8<GT>(cur.r[0], g);
+#pragma unroll
+      for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
+    float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
+    float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+    cur = nxt;
+  }
+  // the (< 8) elements before the aligned body and the (< 8) after it
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) {
+    const int64_t e = tid < a.head ? tid : tail0 + (tid - a.head);
+    step1<GT, PT, F, WRITE_P16>(a, e, gs, bad);
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
 __global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_constant__ StepArgs<MAXR> a) {
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
@@ -345,18 +438,22 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
 // ------------------------------------------------------------------ gradient sum of squares (global clip norm)
 //
 // Deterministic per-shard sum of squares of the reduced gradient. The shard is
-// cut into tiles of kThreads x 8 elements (after the 0..7-element head that
-// aligns the vectors); thread j of a tile owns its 8 consecutive elements and
-// adds their squares in fp32 (a fixed FMA chain), the block combines its
-// threads' sums in double through a fixed shuffle tree, and writes ONE double
-// per tile into the caller's workspace. The head/tail elements (< 16) get a
-// slot of their own. A second one-block kernel adds the slots in index order.
-// The partition depends only on n and the arrays' 16-byte phase, never on the
-// grid size, so the result is bit-reproducible.
+// cut into tiles of kThreads x kSumsqGroups groups of 8 elements (after the
+// 0..7-element head that aligns the vectors); thread j of a tile owns groups
+// j, j + kThreads, ..., issues all their loads first, adds each group's 8
+// squares in fp32 (a fixed FMA chain) and the group sums in double in group
+// order as fp32 pairs (TwoSum); the block combines its threads' pairs through
+// a fixed shuffle tree and writes ONE double per tile into the caller's
+// workspace (GB300's fp64 rate is low, so fp64 is kept to one value per tile). The
+// head/tail elements (< 16) get a slot of their own. A second one-block
+// kernel adds the slots in index order. The partition depends only on n and
+// the arrays' 16-byte phase, never on the grid size, so the result is
+// bit-reproducible.
 //
 // Error: each 8-element fp32 chain of non-negative terms is within 8 * 2^-24
-// relative of its exact value; the double sums add < 2^-40; so the result is
-// within ~5e-7 relative of the exact sum of squares of the fp32 gradients.
+// relative of its exact value; the fp32-pair and double sums add < 2^-40 (the
+// pairs lose at most 2^-48 per addition of non-negative terms); so the result
+// is within ~5e-7 relative of the exact sum of squares of the fp32 gradients.
 
 template <int MAXR>
 struct SumsqArgs {
@@ -372,19 +469,28 @@ struct SumsqArgs {
   float post_scale;
 };
 
-constexpr int kSumsqTile = kThreads * kGroup;
+constexpr int kSumsqGroups = 8;                          // groups per thread per tile
+constexpr int kSumsqTile = kThreads * kGroup * kSumsqGroups;  // elements per tile
 
-__device__ __forceinline__ double block_sum(double x, double* red) {
+// Block-wide sum of per-thread values carried as fp32 pairs (hi + lo, summed
+// with TwoSum through a fixed shuffle tree and a fixed warp order); fp64 only
+// for the block's result. Meaningful in thread 0.
+__device__ __forceinline__ double block_sum(dd x, float2* red) {
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+  for (int off = 16; off > 0; off >>= 1) {
+    const float h = __shfl_xor_sync(0xFFFFFFFFu, x.hi, off);
+    const float l = __shfl_xor_sync(0xFFFFFFFFu, x.lo, off);
+    const dd t = two_sum(x.hi, h);
+    x = {t.hi, t.lo + (x.lo + l)};
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = x;
+  if (lane == 0) red[warp] = make_float2(x.hi, x.lo);
   __syncthreads();
   double s = 0.0;
   if (threadIdx.x == 0)
-    for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+    for (int w = 0; w < kThreads / 32; ++w) s += static_cast<double>(red[w].x) + static_cast<double>(red[w].y);
   __syncthreads();
-  return s;  // meaningful in thread 0
+  return s;
 }
 
 template <int GT, bool FROM_G32, bool VEC, int MAXR>
@@ -395,46 +501,90 @@ __device__ __forceinline__ float reduced1(const SumsqArgs<MAXR>& a, int64_t e) {
   return g;
 }
 
-template <int GT, bool FROM_G32, bool VEC, int MAXR>
+// NR > 0: the rank count as a compile-time constant (N <= 8), which lets the
+// loads of several groups be issued together (batches of ~16 loads per
+// thread); NR == 0: any rank count, one group's ranks at a time.
+template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR>
 __global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
-  __shared__ double red[kThreads / 32];
+  __shared__ float2 red[kThreads / 32];
   const int64_t nvec = (a.n - a.head) / kGroup;
   bool bad = false;
   for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x) {
-    const int64_t gi = tile * kThreads + threadIdx.x;
-    float s = 0.0f;
-    if (gi < nvec) {
-      const int64_t e = a.head + gi * kGroup;
-      float g[8];
-      if constexpr (VEC) {
-        if constexpr (FROM_G32) {
-          ld8f(a.g32 + e, g);
-        } else {
-          reduce8<GT>(a.ranks, a.n_ranks, e, g);
+    // Loads of all groups first, unconditionally: a group past the end reads
+    // group 0 of the shard instead (always in range: ntiles > 0 implies
+    // nvec > 0) and is dropped below, so no branch stands between the loads.
+    float g[kSumsqGroups][8];
+    const int64_t g0 = tile * kSumsqGroups * kThreads + threadIdx.x;
+    if constexpr (VEC && !FROM_G32 && NR > 0) {
+      constexpr int kBatch = NR <= 2 ? 8 : (NR <= 4 ? 4 : 2);  // groups whose loads are issued together
+#pragma unroll
+      for (int q0 = 0; q0 < kSumsqGroups; q0 += kBatch) {
+        uint4 w[kBatch][NR];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          const int64_t gq = g0 + (q0 + b) * kThreads;
+          const int64_t e = a.head + (gq < nvec ? gq : 0) * kGroup;
+#pragma unroll
+          for (int r = 0; r < NR; ++r)
+            w[b][r] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e));
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+          widen8<GT>(w[b][0], g[q0 + b]);
+#pragma unroll
+          for (int r = 1; r < NR; ++r) add8<GT>(w[b][r], g[q0 + b]);
           if (a.post_scale != 1.0f) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+            for (int j = 0; j < 8; ++j) g[q0 + b][j] = g[q0 + b][j] * a.post_scale;
+          }
+        }
+      }
+    } else {
+#pragma unroll
+    for (int q = 0; q < kSumsqGroups; ++q) {
+      const int64_t gq = g0 + q * kThreads;
+      const int64_t e = a.head + (gq < nvec ? gq : 0) * kGroup;
+      if constexpr (VEC) {
+        if constexpr (FROM_G32) {
+          ld8f(a.g32 + e, g[q]);
+        } else {
+          reduce8<GT>(a.ranks, a.n_ranks, e, g[q]);
+          if (a.post_scale != 1.0f) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) g[q][j] = g[q][j] * a.post_scale;
           }
         }
       } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = reduced1<GT, FROM_G32, VEC>(a, e + j);
-      }
-      if (a.g_out) {
-        if constexpr (VEC) {
-          st8f(a.g_out + e, g);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        bad |= !finite(g[j]);
-        s = fmaf(g[j], g[j], s);
+        for (int j = 0; j < 8; ++j) g[q][j] = reduced1<GT, FROM_G32, VEC>(a, e + j);
       }
     }
-    const double t = block_sum(static_cast<double>(s), red);
+    }
+    dd s = {0.0f, 0.0f};  // the thread's group sums, accumulated exactly enough as an fp32 pair
+#pragma unroll
+    for (int q = 0; q < kSumsqGroups; ++q) {
+      const int64_t gi = g0 + q * kThreads;
+      if (gi < nvec) {
+        const int64_t e = a.head + gi * kGroup;
+        if (a.g_out) {
+          if constexpr (VEC) {
+            st8f(a.g_out + e, g[q]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[q][j];
+          }
+        }
+        float c = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          bad |= !finite(g[q][j]);
+          c = fmaf(g[q][j], g[q][j], c);
+        }
+        const dd t = two_sum(s.hi, c);
+        s = {t.hi, s.lo + t.lo};
+      }
+    }
+    const double t = block_sum(s, red);
     if (threadIdx.x == 0) a.partials[tile] = t;
   }
   // head and tail (< 16 elements) in slot ntiles, summed in element order by one thread
@@ -515,19 +665,46 @@ __device__ __forceinline__ uint4 window16(const uint4& c0, const uint4& c1) {
 // read as the two aligned 16-byte chunks that hold it, and only when both
 // chunks lie inside the source range -- otherwise element by element.
 template <int SOFF>
+__device__ __forceinline__ uint4 copy_src16(const char* s, int64_t off, int64_t bytes, int esize, bool& direct) {
+  if constexpr (SOFF == 0) {
+    direct = true;
+    return __ldcs(reinterpret_cast<const uint4*>(s + off));
+  } else {
+    const char* c0 = s + off - SOFF;
+    direct = c0 >= s && (off - SOFF) + 32 <= bytes;
+    if (!direct) return make_uint4(0u, 0u, 0u, 0u);
+    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(c0));
+    const uint4 b = __ldcs(reinterpret_cast<const uint4*>(c0 + 16));
+    return window16<SOFF>(a, b);
+  }
+}
+
+// Body of one segment: destination-aligned 16-byte vectors, kCopyUnroll per
+// thread per iteration with their loads issued first. The source of vector j
+// starts SOFF bytes past a 16-byte boundary; misaligned sources are read as
+// the two aligned 16-byte chunks that hold it, and only when both chunks lie
+// inside the source range -- otherwise element by element.
+constexpr int kCopyUnroll = 4;
+
+template <int SOFF>
 __device__ __forceinline__ void copy_body(const char* s, char* d, int64_t h, int64_t nvec, int64_t bytes, int esize,
                                           int64_t tid, int64_t stride) {
-  for (int64_t j = tid; j < nvec; j += stride) {
-    const int64_t off = h + 16 * j;  // byte offset of this vector in the segment
-    uint4* dv = reinterpret_cast<uint4*>(d + off);
-    if constexpr (SOFF == 0) {
-      __stcs(dv, __ldcs(reinterpret_cast<const uint4*>(s + off)));
-    } else {
-      const char* c0 = s + off - SOFF;
-      if (c0 >= s && (off - SOFF) + 32 <= bytes) {
-        const uint4 a = __ldcs(reinterpret_cast<const uint4*>(c0));
-        const uint4 b = __ldcs(reinterpret_cast<const uint4*>(c0 + 16));
-        __stcs(dv, window16<SOFF>(a, b));
+  for (int64_t j0 = tid; j0 < nvec; j0 += stride * kCopyUnroll) {
+    // all loads first; a vector past the end re-reads vector j0 (in range) and is not stored
+    uint4 v[kCopyUnroll];
+    bool direct[kCopyUnroll];
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t j = j0 + u * stride;
+      v[u] = copy_src16<SOFF>(s, h + 16 * (j < nvec ? j : j0), bytes, esize, direct[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kCopyUnroll; ++u) {
+      const int64_t j = j0 + u * stride;
+      if (j >= nvec) break;
+      const int64_t off = h + 16 * j;
+      if (direct[u]) {
+        __stcs(reinterpret_cast<uint4*>(d + off), v[u]);
       } else {
         for (int i = 0; i < 16; i += esize) {
           if (esize == 2) *reinterpret_cast<uint16_t*>(d + off + i) = *reinterpret_cast<const uint16_t*>(s + off + i);
@@ -676,13 +853,44 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 // ---- dispatch tables (template instantiation by runtime dtype / options)
 
-enum class Path { kScalar, kVector };
+enum class Path { kScalar, kVector, kPipe };
+
+template <int G, int P, bool W, int MAXR, int NR, bool F = false>
+ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
+  auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream);
+}
+
+template <int G, int P, bool W, int MAXR>
+ss_status launch_pipe(const StepArgs<MAXR>& a, void* stream) {
+  switch (a.n_ranks) {
+    case 1: return launch_pipe_n<G, P, W, MAXR, 1>(a, stream);
+    case 2: return launch_pipe_n<G, P, W, MAXR, 2>(a, stream);
+#if SS_PIPE_MAX_RANKS >= 3
+    case 3: return launch_pipe_n<G, P, W, MAXR, 3>(a, stream);
+#endif
+#if SS_PIPE_MAX_RANKS >= 4
+    case 4: return launch_pipe_n<G, P, W, MAXR, 4>(a, stream);
+#endif
+#if SS_PIPE_MAX_RANKS >= 8
+    case 5: return launch_pipe_n<G, P, W, MAXR, 5>(a, stream);
+    case 6: return launch_pipe_n<G, P, W, MAXR, 6>(a, stream);
+    case 7: return launch_pipe_n<G, P, W, MAXR, 7>(a, stream);
+    case 8: return launch_pipe_n<G, P, W, MAXR, 8>(a, stream);
+#endif
+    default: return SS_ERR_INVALID_ARG;
+  }
+}
 
 template <int MAXR>
 ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
                    void* stream) {
 #define SS_ADAM_CASE(G, P, F, W)                                                          \
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
+    if (path == Path::kPipe) {                                                            \
+      if constexpr (F) return launch_pipe_n<G, P, W, MAXR, 2, true>(a, stream);           \
+      else return launch_pipe<G, P, W, MAXR>(a, stream);                                  \
+    }                                                                                     \
     if (path == Path::kVector) {                                                          \
       auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                       \
       return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kStepThreads), a, \
@@ -766,16 +974,32 @@ ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype 
   const unsigned grid = static_cast<unsigned>(
       std::max<int64_t>(1, std::min<int64_t>(a.ntiles, static_cast<int64_t>(sm_count()) * 4)));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-#define SS_SUMSQ_CASE(G, F, V)                                                   \
-  if (gt == G && from_g32 == F && vec == V) sumsq_tiles_kernel<G, F, V, MAXR><<<grid, kThreads, 0, st>>>(a);
-  SS_SUMSQ_CASE(SS_BF16, false, true)
-  else SS_SUMSQ_CASE(SS_BF16, false, false)
-  else SS_SUMSQ_CASE(SS_FP16, false, true)
-  else SS_SUMSQ_CASE(SS_FP16, false, false)
-  else SS_SUMSQ_CASE(SS_BF16, true, true)
-  else SS_SUMSQ_CASE(SS_BF16, true, false)
-  else return SS_ERR_DTYPE;
-#undef SS_SUMSQ_CASE
+  const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
+#define SS_SUMSQ_NR(G, R) \
+  case R: sumsq_tiles_kernel<G, false, true, MAXR, R><<<grid, kThreads, 0, st>>>(a); break;
+#define SS_SUMSQ_RANKED(G)                                                                              \
+  switch (nr) {                                                                                         \
+    SS_SUMSQ_NR(G, 1) SS_SUMSQ_NR(G, 2) SS_SUMSQ_NR(G, 3) SS_SUMSQ_NR(G, 4)                             \
+    SS_SUMSQ_NR(G, 5) SS_SUMSQ_NR(G, 6) SS_SUMSQ_NR(G, 7) SS_SUMSQ_NR(G, 8)                             \
+    default: sumsq_tiles_kernel<G, false, true, MAXR, 0><<<grid, kThreads, 0, st>>>(a);                 \
+  }
+  if (!from_g32 && vec && gt == SS_BF16) {
+    SS_SUMSQ_RANKED(SS_BF16)
+  } else if (!from_g32 && vec && gt == SS_FP16) {
+    SS_SUMSQ_RANKED(SS_FP16)
+  } else if (!from_g32 && gt == SS_BF16) {
+    sumsq_tiles_kernel<SS_BF16, false, false, MAXR, 0><<<grid, kThreads, 0, st>>>(a);
+  } else if (!from_g32 && gt == SS_FP16) {
+    sumsq_tiles_kernel<SS_FP16, false, false, MAXR, 0><<<grid, kThreads, 0, st>>>(a);
+  } else if (from_g32 && vec) {
+    sumsq_tiles_kernel<SS_BF16, true, true, MAXR, 0><<<grid, kThreads, 0, st>>>(a);
+  } else if (from_g32) {
+    sumsq_tiles_kernel<SS_BF16, true, false, MAXR, 0><<<grid, kThreads, 0, st>>>(a);
+  } else {
+    return SS_ERR_DTYPE;
+  }
+#undef SS_SUMSQ_RANKED
+#undef SS_SUMSQ_NR
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   sum_slots_kernel<<<1, 1024, 0, st>>>(a.partials, a.ntiles + 1, out);
@@ -818,7 +1042,7 @@ ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_g
   const bool vec = h >= 0 && h < n;
   const int64_t head = vec ? h : 0;
   const int64_t nvec = (n - head) / kGroup;
-  const int64_t ntiles = (nvec + kThreads - 1) / kThreads;
+  const int64_t ntiles = (nvec + kThreads * kSumsqGroups - 1) / (kThreads * kSumsqGroups);
   auto fill = [&](auto& a) {
     if (!from_g32)
       for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
@@ -946,7 +1170,8 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
   if (n == 0) return SS_OK;
   const int h = common_phase(p16, p32);
   const bool vec = h >= 0 && h < n;
-  const Path path = vec ? Path::kVector : Path::kScalar;
+  const Path path = !vec ? Path::kScalar
+                         : ((from_g32 || n_ranks <= SS_PIPE_MAX_RANKS) ? Path::kPipe : Path::kVector);
   const AdamConst k = make_const(*hp);
   auto fill = [&](auto& a) {
     if (!from_g32)

@@ -213,7 +213,7 @@ ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_no
  * loads the library until the process exits. It allocates nothing and frees
  * nothing. The caller still passes the inputs and outputs, as for
  * ss_grad_sumsq.
- *   - n may be at most SS_NOALLOC_SUMSQ_MAX_N (134,213,632 elements);
+ *   - n may be at most SS_NOALLOC_SUMSQ_MAX_N (1,073,709,056 elements);
  *     larger n returns SS_ERR_OVERFLOW and launches nothing.
  *   - The first call on a device looks up the array's device address with
  *     the runtime (no allocation); make that first call before any stream
@@ -223,7 +223,7 @@ ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_no
  *     Calls ordered on one stream are safe; nothing has to be cleared between
  *     them. */
 #define SS_NOALLOC_SUMSQ_SLOTS 65536
-#define SS_NOALLOC_SUMSQ_MAX_N ((int64_t)(SS_NOALLOC_SUMSQ_SLOTS - 2) * 2048)
+#define SS_NOALLOC_SUMSQ_MAX_N ((int64_t)(SS_NOALLOC_SUMSQ_SLOTS - 2) * 16384)
 ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
                                 ss_dtype gdtype, float post_scale, double* sumsq_out, float* g_out,
                                 int32_t* nonfinite_flag, void* stream);

@@ -137,7 +137,7 @@ def test_reduce_and_copy_argument_errors(ss):
 def test_sumsq_and_clip_argument_errors(ss):
     n = 10_000
     ws = ss.ss_grad_sumsq_workspace(n)
-    assert ws == 8 * ((n + 2047) // 2048 + 2) and ss.ss_grad_sumsq_workspace(-1) == -1
+    assert ws == 8 * ((n + 16383) // 16384 + 2) and ss.ss_grad_sumsq_workspace(-1) == -1
     W, O = 0x70000000, 0x71000000
     with pytest.raises(ss.SSError) as e:            # workspace too small
         ss.ss_grad_sumsq(n, O, W, rank_grads=[A, B], gdtype=ss.SS_BF16, workspace_bytes=ws - 8, stream=0)
@@ -161,4 +161,4 @@ def test_noalloc_size_limit_rejected_on_host(ss):
     with pytest.raises(ss.SSError) as e:
         ss.ss_grad_sumsq_noalloc(ss.SS_NOALLOC_SUMSQ_MAX_N + 1, 0x70000000, g32=0x71000000, stream=0)
     assert e.value.status == 5
-    assert ss.SS_NOALLOC_SUMSQ_MAX_N == (65536 - 2) * 2048
+    assert ss.SS_NOALLOC_SUMSQ_MAX_N == (65536 - 2) * 16384
