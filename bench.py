@@ -415,6 +415,13 @@ def run_suite(args, device) -> dict:
                                        (2 * N + 26) * n)
         out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
         out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
+        if N == 8:
+            # gradient views one element off the state's 16-byte phase: the element-wise path
+            Gm = [g[1:] for g in G]
+            m1 = n - 1
+            out["adam_step_N8_grads_off_by_one"] = entry(
+                timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1]), 5),
+                (2 * N + 26) * m1)
         del G
         torch.cuda.empty_cache()
     del st, p16, g32, ws

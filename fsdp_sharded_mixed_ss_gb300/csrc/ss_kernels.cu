@@ -748,6 +748,128 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
   }
 }
 
+// ------------------------------------------------------------------ fused AdamW step, 16-bit arrays off the state's phase
+//
+// When the fp32 arrays share a 16-byte phase but some 16-bit arrays (rank
+// gradients, param16) do not -- shard views at boundaries that are not
+// multiples of 8 elements, or param16 inside a flat buffer at such a
+// boundary -- groups still start where the fp32 arrays are 16-byte aligned.
+// Every 16-bit gradient array is read as the two aligned 16-byte chunks that
+// hold the group (all loads issued first) and funnel-shifted to its phase;
+// param16 is stored in 4- or 2-byte pieces when it is off phase. The body is groups 1 .. nvec-2, so every chunk read lies inside its
+// array; the first and last groups and the head/tail elements are done one by
+// one.
+template <int MAXR>
+struct ShiftArgs {
+  StepArgs<MAXR> s;
+  uint8_t rphase[MAXR];  // byte offset of each rank's group starts past a 16-byte boundary (even)
+  uint8_t pphase;        // the same for param16
+};
+
+// The 16 bytes that start `phase` bytes into the 32-byte window (a, b).
+__device__ __forceinline__ uint4 window_at(const uint4& a, const uint4& b, int phase) {
+  switch (phase) {
+    case 0: return a;
+    case 2: return window16<2>(a, b);
+    case 4: return window16<4>(a, b);
+    case 6: return window16<6>(a, b);
+    case 8: return window16<8>(a, b);
+    case 10: return window16<10>(a, b);
+    case 12: return window16<12>(a, b);
+    default: return window16<14>(a, b);
+  }
+}
+
+__device__ __forceinline__ void st16_at_phase(void* p, const uint4& v, int phase) {
+  if (phase == 0) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+  } else if ((phase & 3) == 0) {
+    uint32_t* q = static_cast<uint32_t*>(p);
+    q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+  } else {
+    uint16_t* q = static_cast<uint16_t*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+      q[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+    }
+  }
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
+  const StepArgs<MAXR>& a = x.s;
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t g_lo = nvec >= 3 ? 1 : 0, g_hi = nvec >= 3 ? nvec - 1 : 0;  // vector body [g_lo, g_hi)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = g_lo + tid; gi < g_hi; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (FROM_G32) {
+      ld8f(a.g32 + e, g);
+    } else {
+      for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
+        // both aligned chunks around every rank's group, all loads issued before any use
+        // (in the body the second chunk is always inside the array, even at phase 0)
+        uint4 c0[8], c1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (r0 + j < a.n_ranks) {
+            const uint4* c = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + e) - x.rphase[r0 + j]);
+            c0[j] = __ldcs(c);
+            c1[j] = __ldcs(c + 1);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (r0 + j < a.n_ranks) {
+            const uint4 w = window_at(c0[j], c1[j], x.rphase[r0 + j]);
+            if (r0 + j == 0) widen8<GT>(w, g);
+            else add8<GT>(w, g);
+          }
+        }
+      }
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8], m[8], v[8];
+    ld8f(a.master + e, p);
+    ld8f(a.m + e, m);
+    ld8f(a.v + e, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) st16_at_phase(static_cast<uint16_t*>(a.p16) + e, narrow8<PT>(p), x.pphase);
+  }
+  // everything outside the vector body, one element per thread (< 31 elements)
+  const int64_t lo_end = a.head + g_lo * kGroup, hi_start = a.head + g_hi * kGroup;
+  const int64_t n_edge = lo_end + (a.n - hi_start);
+  if (tid < n_edge) step1<GT, PT, FROM_G32, WRITE_P16>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), gs, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
 // ------------------------------------------------------------------ host helpers
 
 struct Range {
@@ -853,7 +975,18 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 // ---- dispatch tables (template instantiation by runtime dtype / options)
 
-enum class Path { kScalar, kVector, kPipe };
+enum class Path { kScalar, kVector, kPipe, kShift };
+
+template <int G, int P, bool F, bool W, int MAXR>
+ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t pphase, void* stream) {
+  ShiftArgs<MAXR> x;
+  std::memset(&x, 0, sizeof x);
+  x.s = a;
+  for (int32_t r = 0; r < a.n_ranks; ++r) x.rphase[r] = rphase[r];
+  x.pphase = pphase;
+  auto* fn = adam_shift_kernel<G, P, F, W, MAXR>;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), x, stream);
+}
 
 template <int G, int P, bool W, int MAXR, int NR, bool F = false>
 ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
@@ -884,9 +1017,10 @@ ss_status launch_pipe(const StepArgs<MAXR>& a, void* stream) {
 
 template <int MAXR>
 ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
-                   void* stream) {
+                   const uint8_t* rphase, uint8_t pphase, void* stream) {
 #define SS_ADAM_CASE(G, P, F, W)                                                          \
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
+    if (path == Path::kShift) return launch_shift<G, P, F, W, MAXR>(a, rphase, pphase, stream); \
     if (path == Path::kPipe) {                                                            \
       if constexpr (F) return launch_pipe_n<G, P, W, MAXR, 2, true>(a, stream);           \
       else return launch_pipe<G, P, W, MAXR>(a, stream);                                  \
@@ -1168,10 +1302,23 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
   }
   if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
   if (n == 0) return SS_OK;
-  const int h = common_phase(p16, p32);
+  int h = common_phase(p16, p32);
   const bool vec = h >= 0 && h < n;
-  const Path path = !vec ? Path::kScalar
-                         : ((from_g32 || n_ranks <= SS_PIPE_MAX_RANKS) ? Path::kPipe : Path::kVector);
+  Path path = !vec ? Path::kScalar : ((from_g32 || n_ranks <= SS_PIPE_MAX_RANKS) ? Path::kPipe : Path::kVector);
+  // 16-bit arrays off the fp32 arrays' phase: per-array byte phases at the fp32 group starts
+  std::vector<uint8_t> rphase(from_g32 ? 0 : n_ranks, 0);
+  uint8_t pphase = 0;
+  if (!vec) {
+    const int h32 = common_phase({}, p32);
+    if (h32 >= 0 && n - h32 >= 3 * kGroup) {
+      h = h32;
+      path = Path::kShift;
+      if (!from_g32)
+        for (int32_t r = 0; r < n_ranks; ++r)
+          rphase[r] = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(rank_grads[r]) + 2u * h) & 15u);
+      if (param16) pphase = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(param16) + 2u * h) & 15u);
+    }
+  }
   const AdamConst k = make_const(*hp);
   auto fill = [&](auto& a) {
     if (!from_g32)
@@ -1186,7 +1333,7 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
     a.dev_scale = o.dev_grad_scale;
     a.dev_skip = o.dev_skip_flag;
     a.n = n;
-    a.head = vec ? h : 0;
+    a.head = path == Path::kScalar ? 0 : h;
     a.n_ranks = from_g32 ? 0 : n_ranks;
     a.post_scale = post_scale;
     a.k = k;
@@ -1197,12 +1344,12 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
     StepArgs<kSmallRanks> a;
     std::memset(&a, 0, sizeof a);
     fill(a);
-    return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, stream);
+    return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, rphase.data(), pphase, stream);
   }
   StepArgs<kLargeRanks> a;
   std::memset(&a, 0, sizeof a);
   fill(a);
-  return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, stream);
+  return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, rphase.data(), pphase, stream);
 }
 
 int64_t ss_grad_sumsq_workspace(int64_t n) {

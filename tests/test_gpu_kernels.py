@@ -279,3 +279,23 @@ def test_step_split_calls_agree(ss):
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+
+
+@pytest.mark.parametrize("goffs,poff", [((1,) * 8, 0), ((0, 1, 2, 3, 4, 5, 6, 7), 3), ((3,) * 8, 1)])
+def test_step_views_off_phase_match_aligned(ss, goffs, poff):
+    """Rank views (and param16) off the state's 16-byte phase take the shifted-load kernel;
+    it must write exactly the bits the aligned kernel writes, and match the oracle."""
+    import torch
+    n, N = (1 << 22) + 3, 8
+    ref = _oracle_step(n, N, synth.BF16, HP)
+    G_al = [dev_bits(s, n) for s in ref[0]]
+    G_off = [dev_bits(s, n, offset=o) for s, o in zip(ref[0], goffs)]
+    a, b = _state(n), _state(n)
+    pa = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    pb = torch.zeros(n + poff, dtype=torch.bfloat16, device="cuda")[poff:]
+    ss.ss_adam_step(HP, n, *a, rank_grads=G_al, param16=pa)
+    ss.ss_adam_step(HP, n, *b, rank_grads=G_off, param16=pb)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+    _check(*b, pb, ref, synth.BF16)
