@@ -64,10 +64,23 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": 6800.0, "source": "fallback"}
 
 
-def profile_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, while the kernel sources still match it."""
+def kernel_fingerprint() -> str:
+    """SHA-256 of the fused step kernel's source: the per-element arithmetic header and the
+    double-buffered kernel's text in the CUDA source (from its comment block to the next kernel)."""
     import hashlib
 
+    src = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "csrc")
+    with open(os.path.join(src, "ss_math.cuh"), "rb") as f:
+        math = f.read()
+    with open(os.path.join(src, "ss_kernels.cu")) as f:
+        text = f.read()
+    start = text.index("// Register double-buffered form for small rank counts")
+    end = text.index("adam_scalar_kernel(", start)
+    return hashlib.sha256(math + text[start:end].encode()).hexdigest()
+
+
+def profile_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, while the kernel's source still matches it."""
     path = os.path.join(ROOT, "profiles", "adam_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -79,13 +92,8 @@ def profile_traffic(kernel: str):
                 ent[k.strip()] = v.strip()
     if ent.get("kernel") != kernel:
         return None
-    src = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "csrc")
-    h = hashlib.sha256()
-    for name in sorted(os.listdir(src)):
-        with open(os.path.join(src, name), "rb") as f:
-            h.update(f.read())
-    if ent.get("csrc_sha256") != h.hexdigest():
-        return None                     # the kernels changed since the counters were taken
+    if ent.get("source_sha256") != kernel_fingerprint():
+        return None                     # the kernel changed since the counters were taken
     return int(ent["dram_bytes_per_launch"])
 
 
