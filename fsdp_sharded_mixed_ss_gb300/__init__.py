@@ -92,6 +92,7 @@ def _load():
     lib.ss_grad_sumsq.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, i64, vp, vp, vp]
     lib.ss_clip_coef.argtypes = [vp, i32, f32, vp, vp, vp]
     lib.ss_grad_sumsq_noalloc.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, vp, vp]
+    lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
     return lib
 
 
@@ -162,6 +163,13 @@ def _ptr_array(xs) -> ctypes.Array:
 
 def ss_abi_version() -> int:
     return int(_lib.ss_abi_version())
+
+
+def ss_device_error(clear: bool = False) -> int:
+    """The library's device error word on the current device (waits for queued work)."""
+    w = ctypes.c_uint32(0)
+    _check(_lib.ss_device_error(ctypes.byref(w), int(bool(clear))), "ss_device_error")
+    return int(w.value)
 
 
 

@@ -238,7 +238,10 @@ ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* 
  *   written at shard_bounds[k]. shard_bounds [n_ranks+1] (host, non-decreasing,
  *   shard_bounds[0] = 0). dtype: SS_BF16, SS_FP16 or SS_FP32. One launch.
  * ss_reshard: the reverse copy, flat -> shards.
- * Bit-exact copies. Shards must not overlap the flat buffer or each other. */
+ * Bit-exact copies. Shards must not overlap the flat buffer or each other.
+ * When every shard and its place in the flat buffer share a 16-byte phase
+ * (and the unit is at least 1 MiB) the copy runs on the bulk-copy (TMA)
+ * engine; otherwise on vector loads and stores. */
 ss_status ss_unshard(const void* const* shards, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
                      void* flat, void* stream);
 ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
@@ -247,6 +250,13 @@ ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ra
 /* ------------------------------------------------------------------- misc */
 const char* ss_status_string(ss_status s);      /* static string, never NULL */
 const char* ss_last_cuda_error(void);           /* last CUDA error text of this thread ("" if none) */
+
+/* The library's device error word on the current device. Bit 0 (value 1): a
+ * bulk-copy wait in an unshard/reshard kernel gave up after about one second
+ * and the kernel returned early, so that copy is incomplete. Copies the word
+ * to *out (host) and, when clear != 0, resets it. Synchronous: it waits for
+ * the work already queued on the device. */
+ss_status ss_device_error(uint32_t* out, int32_t clear);
 int32_t ss_abi_version(void);                   /* SS_ABI_VERSION */
 
 #ifdef __cplusplus
