@@ -72,7 +72,7 @@ def kernel_fingerprint() -> str:
     src = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "csrc")
     with open(os.path.join(src, "ss_math.cuh"), "rb") as f:
         math = f.read()
-    with open(os.path.join(src, "ss_kernels.cu")) as f:
+    with open(os.path.join(src, "ss_step.cu")) as f:
         text = f.read()
     start = text.index("// Register double-buffered form for small rank counts")
     end = text.index("adam_scalar_kernel(", start)
@@ -442,6 +442,14 @@ def run_suite(args, device) -> dict:
         flat = torch.empty(P, dtype=dt, device=device)
         out[name] = entry(timed(lambda: ss.ss_unshard(shards, b, flat)), 4 * P)
         out[name.replace("unshard", "reshard")] = entry(timed(lambda: ss.ss_reshard(flat, b, shards)), 4 * P)
+        if N == 8:
+            # flat buffer one element off the shards' 16-byte phase: the SIMT copy with shifted loads
+            base = torch.empty(P + 8, dtype=dt, device=device)
+            off = base[1:P + 1]
+            out[name + "_flat_off_phase"] = entry(timed(lambda: ss.ss_unshard(shards, b, off)), 4 * P)
+            out[name.replace("unshard", "reshard") + "_flat_off_phase"] = entry(
+                timed(lambda: ss.ss_reshard(off, b, shards)), 4 * P)
+            del base, off
         del shards, flat
         torch.cuda.empty_cache()
     return out

@@ -1,8 +1,9 @@
 """Build step of the shard-step library: compiles csrc/ into libss.so with nvcc for sm_103a.
 
-Two translation units compiled in parallel by nvcc (host layout code and the
-CUDA kernels), linked against the shared CUDA runtime so the library shares
-the runtime instance of the process that loads it (e.g. PyTorch's).
+One translation unit per part of the ABI (host layout code; the fused step;
+the reduce; the norm clip; the copies; shared host helpers), compiled in
+parallel by nvcc and linked against the shared CUDA runtime so the library
+shares the runtime instance of the process that loads it (e.g. PyTorch's).
 """
 from __future__ import annotations
 
@@ -14,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libss.so")
 
-SOURCES = ["ss_layout.cpp", "ss_kernels.cu"]
+SOURCES = ["ss_layout.cpp", "ss_util.cu", "ss_step.cu", "ss_reduce.cu", "ss_norm.cu", "ss_copy.cu"]
 
 
 def nvcc() -> str:
@@ -30,7 +31,7 @@ def build(verbose: bool = False) -> str:
            "-gencode", "arch=compute_103a,code=sm_103a",
            "-fmad=false",                                  # every FMA in the update is explicit
            "-Xcompiler", "-fPIC,-ffp-contract=off",
-           "-cudart", "shared", "--threads", "2",
+           "-cudart", "shared", "--threads", str(len(SOURCES)),
            *[os.path.join(CSRC, s) for s in SOURCES], "-o", LIB]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if verbose and (p.stdout or p.stderr):

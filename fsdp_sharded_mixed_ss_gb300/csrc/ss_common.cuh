@@ -1,0 +1,276 @@
+// ss_common.cuh -- pieces shared by the CUDA sources of the shard-step library:
+// launch constants, 16-bit <-> fp32 vector helpers, the kernels' argument
+// blocks, the rank-ordered gradient sum, and the host-side argument checks.
+//
+// Method ("FSDP: Fully Sharded Data Parallel Training at Scale"): the unit's
+// flat parameter vector is cut into N contiguous shards; in backward the
+// reduce-scatter gives rank k the fp32 sum over ranks of its shard's
+// gradients; the optimizer step then updates the shard's fp32 master, m and v
+// locally; the all-gather concatenates the 16-bit shards into the full unit.
+//
+// Every kernel here is a streaming, HBM-bound pass: no contraction, so no
+// tensor cores. Design for GB300 (sm_103a):
+//   * one thread owns a group of 8 consecutive elements: one 16-byte load per
+//     rank gradient (8 x 16-bit), two 16-byte loads per fp32 state array;
+//     every access is a full 16-byte vector, so each warp moves 512 bytes of
+//     each array per instruction, fully coalesced;
+//   * persistent grid (SM count x resident blocks), grid-stride loop;
+//   * rank gradients are summed in rank order in batches of 8 loads issued
+//     before the adds (8 x 16 B in flight per thread for any N);
+//   * streaming cache hints (evict-first) on read-once and write-once data;
+//   * rank pointer tables travel in the kernel's parameter space
+//     (__grid_constant__), so indexing them costs a constant-bank load;
+//   * odd-length shards and arbitrary views: the first 0..7 elements up to
+//     the common 16-byte phase and the last 0..7 elements are done one by one
+//     by the first threads of the grid; 16-bit arrays off the fp32 arrays'
+//     phase are read as aligned chunk pairs and shifted into place; arrays
+//     with no usable phase at all take the element-wise kernel (same results).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/ss.h"
+#include "ss_math.cuh"
+
+namespace ss {
+
+constexpr int kThreads = 256;
+// Block shape of the fused step kernel (the register-heavy one): threads per
+// block and the minimum resident blocks per SM asked of the compiler.
+#ifndef SS_STEP_THREADS
+#define SS_STEP_THREADS 256
+#endif
+#ifndef SS_STEP_MIN_BLOCKS
+#define SS_STEP_MIN_BLOCKS 1
+#endif
+constexpr int kStepThreads = SS_STEP_THREADS;
+constexpr int kGroup = 8;         // elements per thread per iteration
+constexpr int kSmallRanks = 64;   // pointer table size of the common kernels
+constexpr int kLargeRanks = SS_MAX_RANKS;
+
+// ------------------------------------------------------------------ device helpers
+
+template <int DT>
+__device__ __forceinline__ float widen1(uint16_t h) {
+  if constexpr (DT == SS_BF16) return __uint_as_float(static_cast<uint32_t>(h) << 16);
+  else return __half2float(__ushort_as_half(h));
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t narrow1(float x) {
+  if constexpr (DT == SS_BF16) return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+  else return __half_as_ushort(__float2half_rn(x));
+}
+
+// Two packed 16-bit values (element 0 in the low half) -> two floats.
+template <int DT>
+__device__ __forceinline__ float2 widen2(uint32_t w) {
+  if constexpr (DT == SS_BF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  else {
+    __half2 h;
+    std::memcpy(&h, &w, 4);
+    return __half22float2(h);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t narrow2(float a, float b) {
+  uint32_t w;
+  if constexpr (DT == SS_BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    std::memcpy(&w, &h, 4);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    std::memcpy(&w, &h, 4);
+  }
+  return w;
+}
+
+template <int DT>
+__device__ __forceinline__ void widen8(const uint4& w, float (&f)[8]) {
+  float2 a = widen2<DT>(w.x), b = widen2<DT>(w.y), c = widen2<DT>(w.z), d = widen2<DT>(w.w);
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y; f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+}
+
+template <int DT>
+__device__ __forceinline__ void add8(const uint4& w, float (&f)[8]) {
+  float t[8];
+  widen8<DT>(w, t);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) f[j] = f[j] + t[j];
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 narrow8(const float (&f)[8]) {
+  return make_uint4(narrow2<DT>(f[0], f[1]), narrow2<DT>(f[2], f[3]), narrow2<DT>(f[4], f[5]),
+                    narrow2<DT>(f[6], f[7]));
+}
+
+__device__ __forceinline__ void ld8f(const float* p, float (&f)[8]) {
+  float4 a = __ldcs(reinterpret_cast<const float4*>(p));
+  float4 b = __ldcs(reinterpret_cast<const float4*>(p) + 1);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+__device__ __forceinline__ void st8f(float* p, const float (&f)[8]) {
+  __stcs(reinterpret_cast<float4*>(p), make_float4(f[0], f[1], f[2], f[3]));
+  __stcs(reinterpret_cast<float4*>(p) + 1, make_float4(f[4], f[5], f[6], f[7]));
+}
+
+__device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
+
+// ------------------------------------------------------------------ argument blocks
+
+template <int MAXR>
+struct RankTable {
+  const void* p[MAXR];
+};
+
+template <int MAXR>
+struct StepArgs {
+  RankTable<MAXR> ranks;
+  const float* g32;
+  float* master;
+  float* m;
+  float* v;
+  void* p16;
+  float* g_out;
+  int32_t* nonfinite;
+  const float* dev_scale;
+  const int32_t* dev_skip;
+  int64_t n;
+  int64_t head;  // elements before the first 16-byte-aligned group (vector kernel only)
+  int32_t n_ranks;
+  float post_scale;
+  AdamConst k;
+};
+
+template <int MAXR>
+struct ReduceArgs {
+  RankTable<MAXR> ranks;
+  float* out;
+  int32_t* nonfinite;
+  int64_t n;
+  int64_t head;
+  int32_t n_ranks;
+  float post_scale;
+  int32_t accumulate;
+};
+
+// Sum of the ranks' 8 elements starting at e, in rank order, fp32.
+template <int GT, int MAXR>
+__device__ __forceinline__ void reduce8(const RankTable<MAXR>& t, int n_ranks, int64_t e, float (&g)[8]) {
+  for (int r0 = 0; r0 < n_ranks; r0 += 8) {
+    uint4 w[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (r0 + j < n_ranks) w[j] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(t.p[r0 + j]) + e));
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (r0 + j < n_ranks) {
+        if (r0 + j == 0) widen8<GT>(w[j], g);
+        else add8<GT>(w[j], g);
+      }
+    }
+  }
+}
+
+template <int GT, int MAXR>
+__device__ __forceinline__ float reduce1(const RankTable<MAXR>& t, int n_ranks, int64_t e) {
+  float acc = widen1<GT>(static_cast<const uint16_t*>(t.p[0])[e]);
+  for (int r = 1; r < n_ranks; ++r) acc = acc + widen1<GT>(static_cast<const uint16_t*>(t.p[r])[e]);
+  return acc;
+}
+
+// 16 bytes starting SOFF bytes into the 32-byte window (c0, c1).
+template <int SOFF>
+__device__ __forceinline__ uint4 window16(const uint4& c0, const uint4& c1) {
+  const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  constexpr int q = SOFF / 4;
+  constexpr int r = SOFF % 4;
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (r == 0) o[i] = w[q + i];
+    else o[i] = __funnelshift_r(w[q + i], w[q + i + 1], 8 * r);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Programmatic dependent launch (sm_90 and later). A kernel launched with the
+// programmatic stream serialization attribute (launch_dependent below) may be
+// scheduled before the kernel ahead of it in the stream has finished, once
+// every block of that kernel has called pdl_trigger() or exited. pdl_wait()
+// then holds it until that kernel's grid has completed and its writes are
+// visible -- the hardware's kernel boundary, moved into the kernel; without
+// the attribute it returns at once. Only the launch latency is overlapped:
+// nothing before pdl_wait() may touch memory the previous kernel writes.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Host helpers shared by the entry points (defined in ss_util.cu).
+
+// Byte range of one argument array; `out` marks arrays the call writes.
+struct Range {
+  uintptr_t lo, hi;
+  bool out;
+};
+
+// Text of the last CUDA error seen by this thread (ss_last_cuda_error).
+extern thread_local char g_cuda_err[256];
+// Records `e` as the thread's last CUDA error and returns SS_ERR_CUDA.
+ss_status cuda_fail(cudaError_t e);
+// True when some output byte range overlaps any other range (inputs may overlap inputs).
+bool any_output_overlap(std::vector<Range>& rs);
+Range rng(const void* p, int64_t bytes, bool out);
+// Smallest h in [0, 8) with every 16-bit pointer at a 16-byte boundary after h
+// elements and every fp32 pointer likewise; -1 when none exists.
+int common_phase(const std::vector<uintptr_t>& p16, const std::vector<uintptr_t>& p32);
+int sm_count();
+// Resident blocks per SM of a kernel launched with `threads` per block (cached per kernel).
+int blocks_per_sm(const void* fn, int threads = kThreads);
+// Persistent grid for `work_items` thread-items: at most SM count x resident blocks.
+unsigned grid_for(const void* fn, int64_t work_items, int threads = kThreads);
+// Checks the rank gradient pointers (non-null, 2-byte aligned, 16-bit dtype) and
+// appends their byte ranges and addresses.
+ss_status check_ranks(const void* const* rank_grads, int32_t n_ranks, ss_dtype gdtype, int64_t n,
+                      std::vector<Range>& ranges, std::vector<uintptr_t>& p16);
+
+inline bool is16(ss_dtype d) { return d == SS_BF16 || d == SS_FP16; }
+
+template <typename Args, typename Fn>
+ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream, int threads = kThreads) {
+  fn<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(args);
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+// Launches fn<<<grid, threads, 0, stream>>>(args...) as a programmatic
+// dependent of the previous kernel in the stream (see pdl_wait).
+template <typename... Params, typename... Args>
+ss_status launch_dependent(void (*fn)(Params...), unsigned grid, unsigned threads, void* stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<Params>(args)...);
+  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+}  // namespace ss

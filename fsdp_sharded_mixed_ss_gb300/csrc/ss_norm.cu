@@ -1,0 +1,493 @@
+// ss_norm.cu -- the global gradient-norm clip: the per-shard sum of squares of
+// the reduced gradient (ss_grad_sumsq, and ss_grad_sumsq_noalloc with its slots
+// in a fixed device array) and the clip coefficient from all shards' sums
+// (ss_clip_coef).
+#include "ss_common.cuh"
+
+namespace ss {
+namespace {
+
+// ------------------------------------------------------------------ gradient sum of squares (global clip norm)
+//
+// Deterministic per-shard sum of squares of the reduced gradient. The shard is
+// cut into tiles of kThreads x kSumsqGroups groups of 8 elements (after the
+// 0..7-element head that aligns the vectors); thread j of a tile owns groups
+// j, j + kThreads, ..., issues all their loads first, adds each group's 8
+// squares in fp32 (a fixed FMA chain) and the group sums in double in group
+// order as fp32 pairs (TwoSum); the block combines its threads' pairs through
+// a fixed shuffle tree and writes ONE double per tile into the caller's
+// workspace (GB300's fp64 rate is low, so fp64 is kept to one value per tile). The
+// head/tail elements (< 16) get a slot of their own. A second one-block
+// kernel adds the slots in index order. The partition depends only on n and
+// the arrays' 16-byte phase, never on the grid size, so the result is
+// bit-reproducible.
+//
+// Error: each 8-element fp32 chain of non-negative terms is within 8 * 2^-24
+// relative of its exact value; the fp32-pair and double sums add < 2^-40 (the
+// pairs lose at most 2^-48 per addition of non-negative terms); so the result
+// is within ~5e-7 relative of the exact sum of squares of the fp32 gradients.
+
+template <int MAXR>
+struct SumsqArgs {
+  RankTable<MAXR> ranks;
+  const float* g32;
+  float* g_out;
+  int32_t* nonfinite;
+  double* partials;  // [ntiles + 1]
+  int64_t n;
+  int64_t head;
+  int64_t ntiles;
+  int32_t n_ranks;
+  float post_scale;
+};
+
+constexpr int kSumsqGroups = 8;                          // groups per thread per tile
+constexpr int kSumsqTile = kThreads * kGroup * kSumsqGroups;  // elements per tile
+
+// Block-wide sum of per-thread values carried as fp32 pairs (hi + lo, summed
+// with TwoSum through a fixed shuffle tree, then over the warps in order by
+// thread 0); fp64 only for the block's result, meaningful in thread 0. `red`
+// holds two sets of per-warp slots used on alternate calls (`it` = the
+// block's call count), so one barrier per call suffices: a warp can only
+// write a set again after the next call's barrier, which thread 0 reaches
+// after reading it.
+__device__ __forceinline__ double block_sum(dd x, float2* red, int it) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float h = __shfl_xor_sync(0xFFFFFFFFu, x.hi, off);
+    const float l = __shfl_xor_sync(0xFFFFFFFFu, x.lo, off);
+    const dd t = two_sum(x.hi, h);
+    x = {t.hi, t.lo + (x.lo + l)};
+  }
+  float2* set = red + (it & 1) * (kThreads / 32);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) set[warp] = make_float2(x.hi, x.lo);
+  __syncthreads();
+  double s = 0.0;
+  if (threadIdx.x == 0) {
+    dd acc = {set[0].x, set[0].y};
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) {
+      const dd t = two_sum(acc.hi, set[w].x);
+      acc = {t.hi, t.lo + (acc.lo + set[w].y)};
+    }
+    s = static_cast<double>(acc.hi) + static_cast<double>(acc.lo);
+  }
+  return s;
+}
+
+template <int GT, bool FROM_G32, bool VEC, int MAXR>
+__device__ __forceinline__ float reduced1(const SumsqArgs<MAXR>& a, int64_t e) {
+  if constexpr (FROM_G32) return a.g32[e];
+  float g = reduce1<GT>(a.ranks, a.n_ranks, e);
+  if (a.post_scale != 1.0f) g = g * a.post_scale;
+  return g;
+}
+
+// One reduced group of 8 values at element e: optionally stored to g_out, its
+// squares added in fp32 (a fixed FMA chain), and the sum added to the thread's
+// fp32 pair. The finiteness test runs per element only when the group's sum is
+// not finite (a non-finite value, or squares past the fp32 range).
+template <bool VEC, int MAXR>
+__device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e, const float (&g)[8], dd& s,
+                                            bool& bad) {
+  if (a.g_out) {
+    if constexpr (VEC) {
+      st8f(a.g_out + e, g);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
+    }
+  }
+  float c = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) c = fmaf(g[j], g[j], c);
+  if (!finite(c)) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+  }
+  const dd t = two_sum(s.hi, c);
+  s = {t.hi, s.lo + t.lo};
+}
+
+// Tiles of the compile-time rank count NR (1..8), 16-byte vectors: a block's
+// tiles form one stream of load batches (kB groups x NR ranks per batch),
+// double-buffered in registers -- the loads of batch i+1 are in flight while
+// batch i is converted and squared, and the first batch of the block's next
+// tile is in flight across the tile's block reduction. Batches past the end
+// (of the shard or of the block's tiles) read group 0 instead, always in
+// range, and are dropped, so no branch stands between the loads.
+template <int GT, int MAXR, int NR>
+__device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, float2* red, bool& bad) {
+  constexpr int kB = NR == 2 ? 4 : (NR <= 4 ? 2 : 1);  // groups per batch (measured best on GB300)
+  static_assert(kSumsqGroups % (2 * kB) == 0, "two batches per pipeline round");
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t stride = static_cast<int64_t>(gridDim.x);
+  auto load = [&](uint4 (&w)[kB][NR], int64_t tile, int q0) {
+    const int64_t g0 = tile * kSumsqGroups * kThreads + threadIdx.x;
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      const int64_t gq = g0 + (q0 + b) * kThreads;
+      const int64_t e = a.head + (gq < nvec ? gq : 0) * kGroup;
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        w[b][r] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e));
+    }
+  };
+  auto consume = [&](const uint4 (&w)[kB][NR], int64_t tile, int q0, dd& s) {
+    const int64_t g0 = tile * kSumsqGroups * kThreads + threadIdx.x;
+#pragma unroll
+    for (int b = 0; b < kB; ++b) {
+      float g[8];
+      widen8<GT>(w[b][0], g);
+#pragma unroll
+      for (int r = 1; r < NR; ++r) add8<GT>(w[b][r], g);
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+      const int64_t gq = g0 + (q0 + b) * kThreads;
+      if (gq < nvec) sumsq_group<true>(a, a.head + gq * kGroup, g, s, bad);
+    }
+  };
+  int64_t tile = blockIdx.x;
+  if (tile >= a.ntiles) return;
+  uint4 wa[kB][NR], wb[kB][NR];
+  load(wa, tile, 0);
+  for (int it = 0;; ++it) {
+    const int64_t next = tile + stride < a.ntiles ? tile + stride : tile;
+    dd s = {0.0f, 0.0f};
+#pragma unroll
+    for (int q0 = 0; q0 < kSumsqGroups; q0 += 2 * kB) {
+      load(wb, tile, q0 + kB);
+      consume(wa, tile, q0, s);
+      if (q0 + 2 * kB < kSumsqGroups) load(wa, tile, q0 + 2 * kB);
+      else load(wa, next, 0);
+      consume(wb, tile, q0 + kB, s);
+    }
+    const double t = block_sum(s, red, it);
+    if (threadIdx.x == 0) a.partials[tile] = t;
+    if (next == tile) break;
+    tile = next;
+  }
+}
+
+// NR > 0 (16-bit ranks, 16-byte vectors): the rank count as a compile-time
+// constant (N <= 8), pipelined as above; NR == 0: any rank count, an fp32
+// gradient, or element-wise access -- each thread issues its tile's loads
+// group by group, then squares and sums them.
+template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR>
+__global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
+  __shared__ float2 red[2 * (kThreads / 32)];
+  pdl_trigger();  // the slot sum may be scheduled now; it waits for this grid to finish
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  bool bad = false;
+  if constexpr (VEC && !FROM_G32 && NR > 0) {
+    sumsq_ranked_tiles<GT, MAXR, NR>(a, red, bad);
+  } else {
+    int it = 0;
+    for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
+      // Loads of all groups first, unconditionally: a group past the end reads
+      // group 0 of the shard instead (always in range: ntiles > 0 implies
+      // nvec > 0) and is dropped below, so no branch stands between the loads.
+      float g[kSumsqGroups][8];
+      const int64_t g0 = tile * kSumsqGroups * kThreads + threadIdx.x;
+#pragma unroll
+      for (int q = 0; q < kSumsqGroups; ++q) {
+        const int64_t gq = g0 + q * kThreads;
+        const int64_t e = a.head + (gq < nvec ? gq : 0) * kGroup;
+        if constexpr (VEC) {
+          if constexpr (FROM_G32) {
+            ld8f(a.g32 + e, g[q]);
+          } else {
+            reduce8<GT>(a.ranks, a.n_ranks, e, g[q]);
+            if (a.post_scale != 1.0f) {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) g[q][j] = g[q][j] * a.post_scale;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[q][j] = reduced1<GT, FROM_G32, VEC>(a, e + j);
+        }
+      }
+      dd s = {0.0f, 0.0f};  // the thread's group sums, accumulated exactly enough as an fp32 pair
+#pragma unroll
+      for (int q = 0; q < kSumsqGroups; ++q) {
+        const int64_t gi = g0 + q * kThreads;
+        if (gi < nvec) sumsq_group<VEC>(a, a.head + gi * kGroup, g[q], s, bad);
+      }
+      const double t = block_sum(s, red, it);
+      if (threadIdx.x == 0) a.partials[tile] = t;
+    }
+  }
+  // Head and tail (< 16 elements) in slot ntiles: lane i of the last block's
+  // first warp takes the i-th of them (head first), lane 0 adds the squares
+  // in that order. The last block has the fewest tiles.
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x < 32) {
+    const int64_t tail0 = a.head + nvec * kGroup;
+    const int cnt = static_cast<int>(a.head + (a.n - tail0));
+    const int i = static_cast<int>(threadIdx.x);
+    double x = 0.0;
+    if (i < cnt) {
+      const int64_t e = i < a.head ? i : tail0 + (i - a.head);
+      const float g = reduced1<GT, FROM_G32, VEC>(a, e);
+      if (a.g_out) a.g_out[e] = g;
+      bad |= !finite(g);
+      x = static_cast<double>(fmaf(g, g, 0.0f));
+    }
+    double s = 0.0;
+    for (int j = 0; j < cnt; ++j) s += __shfl_sync(0xFFFFFFFFu, x, j);
+    if (i == 0) a.partials[a.ntiles] = s;
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// out = sum of partials[0..count) in a fixed order, by one block: thread t
+// adds slots t, t + kSlotThreads, ... in that order (eight loads in flight),
+// then a fixed shuffle tree and the warps in order. Launched as a programmatic
+// dependent of the tiles kernel, so its launch overlaps that kernel's end.
+constexpr int kSlotThreads = 256;
+
+__global__ void __launch_bounds__(kSlotThreads) sum_slots_kernel(const double* partials, int64_t count, double* out) {
+  __shared__ double red[kSlotThreads / 32];
+  pdl_wait();
+  pdl_trigger();
+  constexpr int kU = 8;
+  double s = 0.0;
+  for (int64_t base = threadIdx.x; base < count; base += kU * kSlotThreads) {
+    double v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = base + u * kSlotThreads;
+      v[u] = partials[i < count ? i : 0];
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (base + u * kSlotThreads < count) s += v[u];
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double t = 0.0;
+#pragma unroll
+    for (int w = 0; w < kSlotThreads / 32; ++w) t += red[w];
+    *out = t;
+  }
+}
+
+// Global clip coefficient from the shards' sums of squares, added in rank order.
+__global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef,
+                                 double* norm_out) {
+  pdl_wait();
+  pdl_trigger();
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  double total = 0.0;
+  for (int32_t k = 0; k < n_shards; ++k) total += shard_sumsq[k];
+  const double norm = sqrt(total);
+  const double c = static_cast<double>(max_norm) / (norm + 1e-6);
+  *coef = static_cast<float>(c < 1.0 ? c : 1.0);
+  if (norm_out) *norm_out = norm;
+}
+
+template <int MAXR>
+ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // One wave: no more blocks than fit on the GPU at once (the kernel's own
+  // occupancy), so every block takes the same number of tiles within one and
+  // none waits for a free slot while the others finish.
+  auto go = [&](auto* fn) {
+    const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(fn));
+    const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, cap)));
+    fn<<<grid, kThreads, 0, st>>>(a);
+  };
+  const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
+#define SS_SUMSQ_NR(G, R) \
+  case R: go(sumsq_tiles_kernel<G, false, true, MAXR, R>); break;
+// The per-rank-count forms exist for the small rank table only (at most 8 ranks),
+// and an fp32 gradient always travels with the small table.
+#define SS_SUMSQ_RANKED(G)                                                                              \
+  if constexpr (MAXR == kSmallRanks) {                                                                  \
+    switch (nr) {                                                                                       \
+      SS_SUMSQ_NR(G, 1) SS_SUMSQ_NR(G, 2) SS_SUMSQ_NR(G, 3) SS_SUMSQ_NR(G, 4)                           \
+      SS_SUMSQ_NR(G, 5) SS_SUMSQ_NR(G, 6) SS_SUMSQ_NR(G, 7) SS_SUMSQ_NR(G, 8)                           \
+      default: go(sumsq_tiles_kernel<G, false, true, MAXR, 0>);                                         \
+    }                                                                                                   \
+  } else {                                                                                              \
+    go(sumsq_tiles_kernel<G, false, true, MAXR, 0>);                                                    \
+  }
+  if (from_g32) {
+    if constexpr (MAXR != kSmallRanks) return SS_ERR_INVALID_ARG;
+    else if (vec) go(sumsq_tiles_kernel<SS_BF16, true, true, MAXR, 0>);
+    else go(sumsq_tiles_kernel<SS_BF16, true, false, MAXR, 0>);
+  } else if (vec && gt == SS_BF16) {
+    SS_SUMSQ_RANKED(SS_BF16)
+  } else if (vec && gt == SS_FP16) {
+    SS_SUMSQ_RANKED(SS_FP16)
+  } else if (gt == SS_BF16) {
+    go(sumsq_tiles_kernel<SS_BF16, false, false, MAXR, 0>);
+  } else if (gt == SS_FP16) {
+    go(sumsq_tiles_kernel<SS_FP16, false, false, MAXR, 0>);
+  } else {
+    return SS_ERR_DTYPE;
+  }
+#undef SS_SUMSQ_RANKED
+#undef SS_SUMSQ_NR
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return launch_dependent(sum_slots_kernel, 1, kSlotThreads, stream, a.partials, a.ntiles + 1, out);
+}
+
+// Shared by ss_grad_sumsq and any entry point that supplies its own slots.
+ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                          ss_dtype gdtype, float post_scale, double* sumsq_out, double* slots, int64_t slots_bytes,
+                          float* g_out, int32_t* nonfinite_flag, void* stream) {
+  if (n < 0 || !sumsq_out || !slots) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  if (slots_bytes < ss_grad_sumsq_workspace(n)) return SS_ERR_INVALID_ARG;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  const bool from_g32 = g32 != nullptr;
+  if (from_g32) {
+    if (reinterpret_cast<uintptr_t>(g32) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g32, 4 * n, false));
+    p32.push_back(reinterpret_cast<uintptr_t>(g32));
+  } else {
+    ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+    if (st != SS_OK) return st;
+  }
+  if ((reinterpret_cast<uintptr_t>(sumsq_out) & 7u) || (reinterpret_cast<uintptr_t>(slots) & 7u)) return SS_ERR_ALIGN;
+  ranges.push_back(rng(sumsq_out, 8, true));
+  ranges.push_back(rng(slots, ss_grad_sumsq_workspace(n), true));
+  if (g_out) {
+    if (reinterpret_cast<uintptr_t>(g_out) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g_out, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(g_out));
+  }
+  if (nonfinite_flag) {
+    if (reinterpret_cast<uintptr_t>(nonfinite_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(nonfinite_flag, 4, true));
+  }
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  const int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  const int64_t head = vec ? h : 0;
+  const int64_t nvec = (n - head) / kGroup;
+  const int64_t ntiles = (nvec + kThreads * kSumsqGroups - 1) / (kThreads * kSumsqGroups);
+  auto fill = [&](auto& a) {
+    if (!from_g32)
+      for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.g32 = g32;
+    a.g_out = g_out;
+    a.nonfinite = nonfinite_flag;
+    a.partials = slots;
+    a.n = n;
+    a.head = head;
+    a.ntiles = ntiles;
+    a.n_ranks = from_g32 ? 0 : n_ranks;
+    a.post_scale = post_scale;
+  };
+  const ss_dtype gt = from_g32 ? SS_BF16 : gdtype;
+  if (from_g32 || n_ranks <= kSmallRanks) {
+    SumsqArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+  }
+  SumsqArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+int64_t ss_grad_sumsq_workspace(int64_t n) {
+  if (n < 0) return -1;
+  return static_cast<int64_t>(sizeof(double)) * ((n + kSumsqTile - 1) / kSumsqTile + 2);
+}
+
+ss_status ss_grad_sumsq(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                        ss_dtype gdtype, float post_scale, double* sumsq_out, void* workspace,
+                        int64_t workspace_bytes, float* g_out, int32_t* nonfinite_flag, void* stream) {
+  return grad_sumsq_impl(n, g32, rank_grads, n_ranks, gdtype, post_scale, sumsq_out,
+                         static_cast<double*>(workspace), workspace_bytes, g_out, nonfinite_flag, stream);
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- sum of squares without allocation
+//
+// ss_grad_sumsq_noalloc keeps its tile slots in this fixed array instead of a
+// caller workspace, for callers that cannot allocate device memory. Every GPU
+// that loads the library holds the array (SS_NOALLOC_SUMSQ_SLOTS doubles =
+// 512 KiB) until the process exits. All calls share it: each call overwrites
+// every slot it reads before reading it, so nothing needs clearing, but two
+// calls whose kernels overlap on the GPU race on the slots.
+static __device__ __align__(256) double g_noalloc_sumsq_slots[SS_NOALLOC_SUMSQ_SLOTS];
+
+namespace {
+
+// Device address of the slot array on the current device. The name of the
+// array is only a host-side stand-in; the address comes from the runtime, once
+// per device, with that device current.
+ss_status noalloc_slots(double** out) {
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static double* addr[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return SS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_sumsq_slots);
+    if (e != cudaSuccess) return cuda_fail(e);
+    addr[dev] = static_cast<double*>(p);
+  }
+  *out = addr[dev];
+  return SS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* rank_grads, int32_t n_ranks,
+                                ss_dtype gdtype, float post_scale, double* sumsq_out, float* g_out,
+                                int32_t* nonfinite_flag, void* stream) {
+  if (n < 0) return SS_ERR_INVALID_ARG;
+  if (n > SS_NOALLOC_SUMSQ_MAX_N) return SS_ERR_OVERFLOW;
+  double* slots = nullptr;
+  const ss_status st = noalloc_slots(&slots);
+  if (st != SS_OK) return st;
+  return grad_sumsq_impl(n, g32, rank_grads, n_ranks, gdtype, post_scale, sumsq_out, slots,
+                         static_cast<int64_t>(sizeof(double)) * SS_NOALLOC_SUMSQ_SLOTS, g_out, nonfinite_flag,
+                         stream);
+}
+
+ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_norm, float* coef_out,
+                       double* norm_out, void* stream) {
+  if (!shard_sumsq || !coef_out || n_shards < 1 || !(max_norm > 0.0f) || !std::isfinite(max_norm))
+    return SS_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(shard_sumsq) & 7u) || (reinterpret_cast<uintptr_t>(coef_out) & 3u) ||
+      (norm_out && (reinterpret_cast<uintptr_t>(norm_out) & 7u)))
+    return SS_ERR_ALIGN;
+  std::vector<Range> ranges = {rng(shard_sumsq, 8 * static_cast<int64_t>(n_shards), false), rng(coef_out, 4, true)};
+  if (norm_out) ranges.push_back(rng(norm_out, 8, true));
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  return launch_dependent(clip_coef_kernel, 1, 32, stream, shard_sumsq, n_shards, max_norm, coef_out, norm_out);
+}
+
+}  // extern "C"

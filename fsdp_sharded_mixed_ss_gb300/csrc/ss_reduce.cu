@@ -1,0 +1,131 @@
+// ss_reduce.cu -- the standalone virtual-rank gradient reduce (ss_grad_reduce):
+// the fp32 rank-ordered sum of the ranks' 16-bit gradient shards, optionally
+// scaled, accumulated into the output and checked for non-finite values.
+#include "ss_common.cuh"
+
+namespace ss {
+namespace {
+
+// ------------------------------------------------------------------ gradient reduce
+
+template <int GT, int MAXR>
+__device__ __forceinline__ void reduce_one(const ReduceArgs<MAXR>& a, int64_t e, bool& bad) {
+  float g = reduce1<GT>(a.ranks, a.n_ranks, e);
+  if (a.post_scale != 1.0f) g = g * a.post_scale;
+  if (a.accumulate) g = a.out[e] + g;
+  bad |= !finite(g);
+  a.out[e] = g;
+}
+
+template <int GT, int MAXR>
+__global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    reduce8<GT>(a.ranks, a.n_ranks, e, g);
+    if (a.post_scale != 1.0f) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+    }
+    if (a.accumulate) {
+      float o[8];
+      ld8f(a.out + e, o);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = o[j] + g[j];
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    st8f(a.out + e, g);
+  }
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) reduce_one<GT>(a, tid < a.head ? tid : tail0 + (tid - a.head), bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int GT, int MAXR>
+__global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t e = tid; e < a.n; e += stride) reduce_one<GT>(a, e, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int MAXR>
+ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* stream) {
+#define SS_RED_CASE(G)                                                                     \
+  if (gt == G) {                                                                           \
+    if (vec) {                                                                             \
+      auto* fn = reduce_vec_kernel<G, MAXR>;                                               \
+      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
+    }                                                                                      \
+    auto* fn = reduce_scalar_kernel<G, MAXR>;                                              \
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), a.n), a, stream);        \
+  }
+  SS_RED_CASE(SS_BF16)
+  SS_RED_CASE(SS_FP16)
+#undef SS_RED_CASE
+  return SS_ERR_DTYPE;
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtype gdtype, int64_t n,
+                         float post_scale, int32_t accumulate, float* g_out, int32_t* nonfinite_flag,
+                         void* stream) {
+  if (n < 0) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+  if (st != SS_OK) return st;
+  if (!g_out) return SS_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(g_out) & 3u) return SS_ERR_ALIGN;
+  if (nonfinite_flag && (reinterpret_cast<uintptr_t>(nonfinite_flag) & 3u)) return SS_ERR_ALIGN;
+  ranges.push_back(rng(g_out, 4 * n, true));
+  if (nonfinite_flag) ranges.push_back(rng(nonfinite_flag, 4, true));
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  if (n == 0) return SS_OK;
+  p32.push_back(reinterpret_cast<uintptr_t>(g_out));
+  const int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  auto fill = [&](auto& a) {
+    for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.out = g_out;
+    a.nonfinite = nonfinite_flag;
+    a.n = n;
+    a.head = vec ? h : 0;
+    a.n_ranks = n_ranks;
+    a.post_scale = post_scale;
+    a.accumulate = accumulate != 0;
+  };
+  if (n_ranks <= kSmallRanks) {
+    ReduceArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_reduce(a, vec, gdtype, stream);
+  }
+  ReduceArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_reduce(a, vec, gdtype, stream);
+}
+
+}  // extern "C"

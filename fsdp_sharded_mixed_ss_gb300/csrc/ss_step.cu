@@ -1,0 +1,535 @@
+// ss_step.cu -- the fused shard step (ss_adam_step): rank-ordered fp32 reduce of
+// the ranks' gradient shards, AdamW on the fp32 master and moments, and the
+// 16-bit parameter cast, in one pass over HBM. Four kernel forms share the
+// per-element arithmetic of ss_math.cuh: register double-buffered (up to 8
+// ranks or an fp32 gradient), single-buffered vector (more ranks), shifted
+// loads (16-bit arrays off the state's 16-byte phase) and element-wise.
+#include "ss_common.cuh"
+
+namespace ss {
+namespace {
+
+// ------------------------------------------------------------------ fused AdamW step
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float gs, bool& bad) {
+  float g;
+  if constexpr (FROM_G32) {
+    g = a.g32[e];
+  } else {
+    g = reduce1<GT>(a.ranks, a.n_ranks, e);
+    if (a.post_scale != 1.0f) g = g * a.post_scale;
+  }
+  bad |= !finite(g);
+  if (a.g_out) a.g_out[e] = g;
+  if (a.dev_scale) g = g * gs;
+  float p = a.master[e], m = a.m[e], v = a.v[e];
+  adamw_elem(a.k, g, p, m, v);
+  a.master[e] = p;
+  a.m[e] = m;
+  a.v[e] = v;
+  if constexpr (WRITE_P16) static_cast<uint16_t*>(a.p16)[e] = narrow1<PT>(p);
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (FROM_G32) {
+      ld8f(a.g32 + e, g);
+    } else {
+      reduce8<GT>(a.ranks, a.n_ranks, e, g);
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8], m[8], v[8];
+    ld8f(a.master + e, p);
+    ld8f(a.m + e, m);
+    ld8f(a.v + e, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+  }
+  // the (< 8) elements before the aligned body and the (< 8) after it
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) {
+    const int64_t e = tid < a.head ? tid : tail0 + (tid - a.head);
+    step1<GT, PT, FROM_G32, WRITE_P16>(a, e, gs, bad);
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// Register double-buffered form for small rank counts: the loads of a
+// thread's next group are issued before the update of its current group, so
+// each thread keeps two groups of bytes in flight (for N <= SS_PIPE_MAX_RANKS,
+// where one group alone is too few bytes to cover HBM latency at the
+// residency the update's registers allow). NR is the rank count; with F the
+// gradient is the fp32 array g32, held as NR = 2 raw 16-byte chunks.
+#ifndef SS_PIPE_MAX_RANKS
+#define SS_PIPE_MAX_RANKS 8
+#endif
+template <int NR>
+struct PipeGroup {
+  uint4 r[NR];
+  float4 s[6];  // master, m, v: two float4 each
+};
+
+template <int GT, int NR, bool F, int MAXR>
+__device__ __forceinline__ void pipe_load(const StepArgs<MAXR>& a, int64_t gi, PipeGroup<NR>& G) {
+  const int64_t e = a.head + gi * kGroup;
+  if constexpr (F) {
+    static_assert(NR == 2, "the fp32 gradient occupies two chunks");
+    G.r[0] = __ldcs(reinterpret_cast<const uint4*>(a.g32 + e));
+    G.r[1] = __ldcs(reinterpret_cast<const uint4*>(a.g32 + e) + 1);
+  } else {
+#pragma unroll
+    for (int r = 0; r < NR; ++r) G.r[r] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e));
+  }
+  G.s[0] = __ldcs(reinterpret_cast<const float4*>(a.master + e));
+  G.s[1] = __ldcs(reinterpret_cast<const float4*>(a.master + e) + 1);
+  G.s[2] = __ldcs(reinterpret_cast<const float4*>(a.m + e));
+  G.s[3] = __ldcs(reinterpret_cast<const float4*>(a.m + e) + 1);
+  G.s[4] = __ldcs(reinterpret_cast<const float4*>(a.v + e));
+  G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + e) + 1);
+}
+
+template <int GT, int PT, bool F, bool WRITE_P16, int MAXR, int NR>
+__global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  PipeGroup<NR> cur, nxt;
+  if (tid < nvec) pipe_load<GT, NR, F>(a, tid, cur);
+  for (int64_t gi = tid; gi < nvec; gi += stride) {
+    if (gi + stride < nvec) pipe_load<GT, NR, F>(a, gi + stride, nxt);
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (F) {
+      const uint4 x = cur.r[0], y = cur.r[1];
+      g[0] = __uint_as_float(x.x); g[1] = __uint_as_float(x.y); g[2] = __uint_as_float(x.z); g[3] = __uint_as_float(x.w);
+      g[4] = __uint_as_float(y.x); g[5] = __uint_as_float(y.y); g[6] = __uint_as_float(y.z); g[7] = __uint_as_float(y.w);
+    } else {
+      widen8<GT>(cur.r[0], g);
+#pragma unroll
+      for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
+    float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
+    float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+    cur = nxt;
+  }
+  // the (< 8) elements before the aligned body and the (< 8) after it
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) {
+    const int64_t e = tid < a.head ? tid : tail0 + (tid - a.head);
+    step1<GT, PT, F, WRITE_P16>(a, e, gs, bad);
+  }
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t e = tid; e < a.n; e += stride) step1<GT, PT, FROM_G32, WRITE_P16>(a, e, gs, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// ------------------------------------------------------------------ fused AdamW step, 16-bit arrays off the state's phase
+//
+// When the fp32 arrays share a 16-byte phase but some 16-bit arrays (rank
+// gradients, param16) do not -- shard views at boundaries that are not
+// multiples of 8 elements, or param16 inside a flat buffer at such a
+// boundary -- groups still start where the fp32 arrays are 16-byte aligned.
+// Every 16-bit gradient array is read as the two aligned 16-byte chunks that
+// hold the group (all loads issued first) and funnel-shifted to its phase;
+// param16 is stored in 4- or 2-byte pieces when it is off phase. The body is groups 1 .. nvec-2, so every chunk read lies inside its
+// array; the first and last groups and the head/tail elements are done one by
+// one.
+template <int MAXR>
+struct ShiftArgs {
+  StepArgs<MAXR> s;
+  uint8_t rphase[MAXR];  // byte offset of each rank's group starts past a 16-byte boundary (even)
+  uint8_t pphase;        // the same for param16
+};
+
+// The 16 bytes that start `phase` bytes into the 32-byte window (a, b).
+__device__ __forceinline__ uint4 window_at(const uint4& a, const uint4& b, int phase) {
+  switch (phase) {
+    case 0: return a;
+    case 2: return window16<2>(a, b);
+    case 4: return window16<4>(a, b);
+    case 6: return window16<6>(a, b);
+    case 8: return window16<8>(a, b);
+    case 10: return window16<10>(a, b);
+    case 12: return window16<12>(a, b);
+    default: return window16<14>(a, b);
+  }
+}
+
+__device__ __forceinline__ void st16_at_phase(void* p, const uint4& v, int phase) {
+  if (phase == 0) {
+    __stcs(reinterpret_cast<uint4*>(p), v);
+  } else if ((phase & 3) == 0) {
+    uint32_t* q = static_cast<uint32_t*>(p);
+    q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
+  } else {
+    uint16_t* q = static_cast<uint16_t*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      q[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
+      q[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
+    }
+  }
+}
+
+template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
+__global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
+  const StepArgs<MAXR>& a = x.s;
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t g_lo = nvec >= 3 ? 1 : 0, g_hi = nvec >= 3 ? nvec - 1 : 0;  // vector body [g_lo, g_hi)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  bool bad = false;
+  for (int64_t gi = g_lo + tid; gi < g_hi; gi += stride) {
+    const int64_t e = a.head + gi * kGroup;
+    float g[8];
+    if constexpr (FROM_G32) {
+      ld8f(a.g32 + e, g);
+    } else {
+      for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
+        // both aligned chunks around every rank's group, all loads issued before any use
+        // (in the body the second chunk is always inside the array, even at phase 0)
+        uint4 c0[8], c1[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (r0 + j < a.n_ranks) {
+            const uint4* c = reinterpret_cast<const uint4*>(
+                reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + e) - x.rphase[r0 + j]);
+            c0[j] = __ldcs(c);
+            c1[j] = __ldcs(c + 1);
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (r0 + j < a.n_ranks) {
+            const uint4 w = window_at(c0[j], c1[j], x.rphase[r0 + j]);
+            if (r0 + j == 0) widen8<GT>(w, g);
+            else add8<GT>(w, g);
+          }
+        }
+      }
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+    }
+    if (a.nonfinite) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+    }
+    if (a.g_out) st8f(a.g_out + e, g);
+    if (a.dev_scale) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+    }
+    float p[8], m[8], v[8];
+    ld8f(a.master + e, p);
+    ld8f(a.m + e, m);
+    ld8f(a.v + e, v);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+    st8f(a.master + e, p);
+    st8f(a.m + e, m);
+    st8f(a.v + e, v);
+    if constexpr (WRITE_P16) st16_at_phase(static_cast<uint16_t*>(a.p16) + e, narrow8<PT>(p), x.pphase);
+  }
+  // everything outside the vector body, one element per thread (< 31 elements)
+  const int64_t lo_end = a.head + g_lo * kGroup, hi_start = a.head + g_hi * kGroup;
+  const int64_t n_edge = lo_end + (a.n - hi_start);
+  if (tid < n_edge) step1<GT, PT, FROM_G32, WRITE_P16>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), gs, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
+// Splits a double into an fp32 pair hi + lo (hi = nearest float, lo = nearest float to the rest).
+void split(double x, float& hi, float& lo) {
+  hi = static_cast<float>(x);
+  lo = static_cast<float>(x - static_cast<double>(hi));
+}
+
+AdamConst make_const(const ss_adamw_hparams& hp) {
+  const double b1 = hp.beta1, b2 = hp.beta2;
+  const double bc1 = 1.0 - std::pow(b1, static_cast<double>(hp.step));
+  const double bc2 = 1.0 - std::pow(b2, static_cast<double>(hp.step));
+  const double sq = std::sqrt(bc2);
+  AdamConst k;
+  k.b1 = hp.beta1;
+  split(1.0 - b1, k.c1, k.c1_lo);
+  k.b2 = hp.beta2;
+  split(1.0 - b2, k.c2, k.c2_lo);
+  split(static_cast<double>(hp.lr) * sq / bc1, k.A_hi, k.A_lo);
+  split(static_cast<double>(hp.eps) * sq, k.E_hi, k.E_lo);
+  split(1.0 - static_cast<double>(hp.lr) * static_cast<double>(hp.weight_decay), k.D_hi, k.D_lo);
+  return k;
+}
+
+bool valid_hp(const ss_adamw_hparams* hp) {
+  if (!hp || hp->step < 1) return false;
+  const float f[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+  for (float x : f)
+    if (!std::isfinite(x) || x < 0.0f) return false;
+  return hp->beta1 < 1.0f && hp->beta2 < 1.0f;
+}
+
+// ---- dispatch tables (template instantiation by runtime dtype / options)
+
+enum class Path { kScalar, kVector, kPipe, kShift };
+
+template <int G, int P, bool F, bool W, int MAXR>
+ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t pphase, void* stream) {
+  ShiftArgs<MAXR> x;
+  std::memset(&x, 0, sizeof x);
+  x.s = a;
+  for (int32_t r = 0; r < a.n_ranks; ++r) x.rphase[r] = rphase[r];
+  x.pphase = pphase;
+  auto* fn = adam_shift_kernel<G, P, F, W, MAXR>;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), x, stream);
+}
+
+template <int G, int P, bool W, int MAXR, int NR, bool F = false>
+ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
+  auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream);
+}
+
+template <int G, int P, bool W, int MAXR>
+ss_status launch_pipe(const StepArgs<MAXR>& a, void* stream) {
+  switch (a.n_ranks) {
+    case 1: return launch_pipe_n<G, P, W, MAXR, 1>(a, stream);
+    case 2: return launch_pipe_n<G, P, W, MAXR, 2>(a, stream);
+#if SS_PIPE_MAX_RANKS >= 3
+    case 3: return launch_pipe_n<G, P, W, MAXR, 3>(a, stream);
+#endif
+#if SS_PIPE_MAX_RANKS >= 4
+    case 4: return launch_pipe_n<G, P, W, MAXR, 4>(a, stream);
+#endif
+#if SS_PIPE_MAX_RANKS >= 8
+    case 5: return launch_pipe_n<G, P, W, MAXR, 5>(a, stream);
+    case 6: return launch_pipe_n<G, P, W, MAXR, 6>(a, stream);
+    case 7: return launch_pipe_n<G, P, W, MAXR, 7>(a, stream);
+    case 8: return launch_pipe_n<G, P, W, MAXR, 8>(a, stream);
+#endif
+    default: return SS_ERR_INVALID_ARG;
+  }
+}
+
+template <int MAXR>
+ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
+                   const uint8_t* rphase, uint8_t pphase, void* stream) {
+  // Only reachable forms are instantiated: an fp32 gradient (gt is then the
+  // placeholder SS_BF16) always travels with the small rank table and takes the
+  // double-buffered, shifted or element-wise form; the double-buffered form is
+  // chosen only for at most SS_PIPE_MAX_RANKS ranks, so only with the small table.
+#define SS_ADAM_CASE(G, P, F, W)                                                          \
+  if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
+    if (path == Path::kShift) return launch_shift<G, P, F, W, MAXR>(a, rphase, pphase, stream); \
+    if (path == Path::kPipe) {                                                            \
+      if constexpr (MAXR != kSmallRanks) return SS_ERR_INVALID_ARG;                       \
+      else if constexpr (F) return launch_pipe_n<G, P, W, MAXR, 2, true>(a, stream);      \
+      else return launch_pipe<G, P, W, MAXR>(a, stream);                                  \
+    }                                                                                     \
+    if (path == Path::kVector) {                                                          \
+      if constexpr (F) return SS_ERR_INVALID_ARG;                                         \
+      else {                                                                              \
+        auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                     \
+        return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kStepThreads), a, \
+                      stream, kStepThreads);                                              \
+      }                                                                                   \
+    }                                                                                     \
+    auto* fn = adam_scalar_kernel<G, P, F, W, MAXR>;                                      \
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), a.n), a, stream);       \
+  }
+#define SS_ADAM_P(G, P) SS_ADAM_CASE(G, P, false, true) SS_ADAM_CASE(G, P, false, false)
+  SS_ADAM_P(SS_BF16, SS_BF16)
+  SS_ADAM_P(SS_BF16, SS_FP16)
+  SS_ADAM_P(SS_FP16, SS_BF16)
+  SS_ADAM_P(SS_FP16, SS_FP16)
+  if constexpr (MAXR == kSmallRanks) {
+    SS_ADAM_CASE(SS_BF16, SS_BF16, true, true)
+    SS_ADAM_CASE(SS_BF16, SS_BF16, true, false)
+    SS_ADAM_CASE(SS_BF16, SS_FP16, true, true)
+    SS_ADAM_CASE(SS_BF16, SS_FP16, true, false)
+  }
+#undef SS_ADAM_P
+#undef SS_ADAM_CASE
+  return SS_ERR_DTYPE;
+}
+
+}  // namespace
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, const void* const* rank_grads,
+                       int32_t n_ranks, ss_dtype gdtype, float post_scale, float* master, float* m, float* v,
+                       void* param16, ss_dtype pdtype, const ss_step_options* opts, void* stream) {
+  if (!valid_hp(hp) || n < 0) return SS_ERR_INVALID_ARG;
+  if (n > INT64_MAX / 16) return SS_ERR_OVERFLOW;
+  if (!master || !m || !v) return SS_ERR_INVALID_ARG;
+  std::vector<Range> ranges;
+  std::vector<uintptr_t> p16, p32;
+  const bool from_g32 = g32 != nullptr;
+  if (from_g32) {
+    if (reinterpret_cast<uintptr_t>(g32) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(g32, 4 * n, false));
+    p32.push_back(reinterpret_cast<uintptr_t>(g32));
+  } else {
+    ss_status st = check_ranks(rank_grads, n_ranks, gdtype, n, ranges, p16);
+    if (st != SS_OK) return st;
+  }
+  for (const float* p : {static_cast<const float*>(master), static_cast<const float*>(m), static_cast<const float*>(v)}) {
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(p, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(p));
+  }
+  if (param16) {
+    if (!is16(pdtype)) return SS_ERR_DTYPE;
+    if (reinterpret_cast<uintptr_t>(param16) & 1u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(param16, 2 * n, true));
+    p16.push_back(reinterpret_cast<uintptr_t>(param16));
+  }
+  ss_step_options o{};
+  if (opts) o = *opts;
+  if (o.g_out) {
+    if (reinterpret_cast<uintptr_t>(o.g_out) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.g_out, 4 * n, true));
+    p32.push_back(reinterpret_cast<uintptr_t>(o.g_out));
+  }
+  if (o.nonfinite_flag) {
+    if (reinterpret_cast<uintptr_t>(o.nonfinite_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.nonfinite_flag, 4, true));
+  }
+  if (o.dev_grad_scale) {
+    if (reinterpret_cast<uintptr_t>(o.dev_grad_scale) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.dev_grad_scale, 4, false));
+  }
+  if (o.dev_skip_flag) {
+    if (reinterpret_cast<uintptr_t>(o.dev_skip_flag) & 3u) return SS_ERR_ALIGN;
+    ranges.push_back(rng(o.dev_skip_flag, 4, false));
+  }
+  if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
+  if (n == 0) return SS_OK;
+  int h = common_phase(p16, p32);
+  const bool vec = h >= 0 && h < n;
+  Path path = !vec ? Path::kScalar : ((from_g32 || n_ranks <= SS_PIPE_MAX_RANKS) ? Path::kPipe : Path::kVector);
+  // 16-bit arrays off the fp32 arrays' phase: per-array byte phases at the fp32 group starts
+  std::vector<uint8_t> rphase(from_g32 ? 0 : n_ranks, 0);
+  uint8_t pphase = 0;
+  if (!vec) {
+    const int h32 = common_phase({}, p32);
+    if (h32 >= 0 && n - h32 >= 3 * kGroup) {
+      h = h32;
+      path = Path::kShift;
+      if (!from_g32)
+        for (int32_t r = 0; r < n_ranks; ++r)
+          rphase[r] = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(rank_grads[r]) + 2u * h) & 15u);
+      if (param16) pphase = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(param16) + 2u * h) & 15u);
+    }
+  }
+  const AdamConst k = make_const(*hp);
+  auto fill = [&](auto& a) {
+    if (!from_g32)
+      for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
+    a.g32 = g32;
+    a.master = master;
+    a.m = m;
+    a.v = v;
+    a.p16 = param16;
+    a.g_out = o.g_out;
+    a.nonfinite = o.nonfinite_flag;
+    a.dev_scale = o.dev_grad_scale;
+    a.dev_skip = o.dev_skip_flag;
+    a.n = n;
+    a.head = path == Path::kScalar ? 0 : h;
+    a.n_ranks = from_g32 ? 0 : n_ranks;
+    a.post_scale = post_scale;
+    a.k = k;
+  };
+  const ss_dtype gt = from_g32 ? SS_BF16 : gdtype;
+  const ss_dtype pt = param16 ? pdtype : SS_BF16;
+  if (from_g32 || n_ranks <= kSmallRanks) {
+    StepArgs<kSmallRanks> a;
+    std::memset(&a, 0, sizeof a);
+    fill(a);
+    return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, rphase.data(), pphase, stream);
+  }
+  StepArgs<kLargeRanks> a;
+  std::memset(&a, 0, sizeof a);
+  fill(a);
+  return run_adam(a, path, from_g32, param16 != nullptr, gt, pt, rphase.data(), pphase, stream);
+}
+
+}  // extern "C"

@@ -185,7 +185,9 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
  *   needed). Each group of 8 squares is added in fp32, the rest in double, in
  *   an order fixed by n and the arrays' alignment (not by the launch), so the
  *   result is reproducible and within 5e-7 relative of the exact sum.
- *   Two kernel launches on `stream`.
+ *   Two kernel launches on `stream`; the second (the final sum over the
+ *   tiles) is a programmatic dependent of the first, so its launch overlaps
+ *   the first's end (it still reads nothing before the first has finished).
  * ss_grad_sumsq_workspace: the workspace size in bytes for a shard of n
  *   elements (-1 if n < 0).
  * ss_clip_coef: shard_sumsq [n_shards] (device doubles, one per shard) ->

@@ -61,6 +61,27 @@ def test_sumsq_matches_oracle(ss, N, n, fmt):
     assert abs(out.item() - ref) <= 1e-6 * ref
 
 
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8])
+def test_sumsq_several_tiles_per_block(ss, N):
+    """2^24 + 5 elements: more tiles than blocks, so each block runs its pipelined loads across
+    several tiles (and the last ones read past their tiles' ends), with a ragged 5-element tail."""
+    import torch
+    n = (1 << 24) + 5
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 9) for r in range(N)]
+    G = [dev_bits(s, n) for s in specs]
+    out = torch.zeros(1, dtype=torch.float64, device="cuda")
+    g_out = torch.empty(n, dtype=torch.float32, device="cuda")
+    ws = workspace(ss, n)
+    ss.ss_grad_sumsq(n, out, ws, rank_grads=G, post_scale=0.25, g_out=g_out)
+    g = oracle.grad_reduce([synth.host_range(s, 0, n) for s in specs], oracle.BF16, post_scale=0.25)
+    assert np.array_equal(g_out.cpu().numpy().view(np.uint32), g.view(np.uint32))
+    ref = oracle.sumsq(g)
+    assert abs(out.item() - ref) <= 1e-6 * ref
+    again = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ss.ss_grad_sumsq(n, again, ws, rank_grads=G, post_scale=0.25)
+    assert again.item() == out.item()
+
+
 def test_sumsq_from_fp32_and_reproducible(ss):
     import torch
     n = 3_000_017
