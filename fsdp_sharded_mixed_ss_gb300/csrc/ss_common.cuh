@@ -248,29 +248,35 @@ ss_status check_ranks(const void* const* rank_grads, int32_t n_ranks, ss_dtype g
 
 inline bool is16(ss_dtype d) { return d == SS_BF16 || d == SS_FP16; }
 
-template <typename Args, typename Fn>
-ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream, int threads = kThreads) {
-  fn<<<grid, threads, 0, static_cast<cudaStream_t>(stream)>>>(args);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SS_OK : cuda_fail(e);
-}
 
-// Launches fn<<<grid, threads, 0, stream>>>(args...) as a programmatic
-// dependent of the previous kernel in the stream (see pdl_wait).
+// Launches fn<<<grid, block, smem, stream>>>(args...) as a programmatic
+// dependent of the previous kernel in the stream (see pdl_wait). Every kernel
+// of the library starts with pdl_wait() and pdl_trigger(), and every grid is
+// at most one wave, so all of a grid's blocks are resident before any of them
+// lets the next kernel launch.
 template <typename... Params, typename... Args>
-ss_status launch_dependent(void (*fn)(Params...), unsigned grid, unsigned threads, void* stream, Args... args) {
+ss_status launch_dependent(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem, void* stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+#ifdef SS_NO_PDL
+  cfg.numAttrs = 0;
+#else
   cfg.numAttrs = 1;
+#endif
   const cudaError_t e = cudaLaunchKernelEx(&cfg, fn, static_cast<Params>(args)...);
   return e == cudaSuccess ? SS_OK : cuda_fail(e);
+}
+
+template <typename Args, typename Fn>
+ss_status launch(Fn* fn, unsigned grid, const Args& args, void* stream, int threads = kThreads) {
+  return launch_dependent(fn, dim3(grid), dim3(static_cast<unsigned>(threads)), 0, stream, args);
 }
 
 }  // namespace ss

@@ -75,6 +75,8 @@ __device__ __forceinline__ void copy_body(const char* s, char* d, int64_t h, int
 
 template <int MAXR>
 __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_constant__ CopyArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   const int k = blockIdx.y;
   const int64_t bytes = a.bytes[k];
   if (bytes == 0) return;
@@ -195,6 +197,8 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 template <int MAXR>
 __global__ void __launch_bounds__(32) copy_tma_kernel(const __grid_constant__ CopyArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ __align__(128) unsigned char buf[];  // [kTmaSlots][kTmaChunk]
   __shared__ __align__(8) uint64_t bars[kTmaSlots];
   const int k = blockIdx.y;
@@ -279,7 +283,6 @@ ss_status run_copy(const void* const* src, void* const* dst, const int64_t* byte
   }
   a.n_seg = n_seg;
   a.esize = esize;
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (same_phase && total_bytes >= (int64_t{1} << 20)) {
     // bulk-copy engine: one-warp blocks, kTmaSlots chunks in flight each
     auto* fn = copy_tma_kernel<MAXR>;
@@ -291,19 +294,14 @@ ss_status run_copy(const void* const* src, void* const* dst, const int64_t* byte
     const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
     const int64_t chunks = (total_bytes / std::max(1, n_seg)) / kTmaChunk + 1;
     const int64_t gx = std::max<int64_t>(1, std::min<int64_t>((cap + n_seg - 1) / n_seg, chunks));
-    fn<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg)), 32, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? SS_OK : cuda_fail(e);
+    return launch_dependent(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg)), dim3(32), smem, stream, a);
   }
   auto* fn = copy_segments_kernel<MAXR>;
   const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(fn)));
   const int64_t per_seg_work = (total_bytes / std::max(1, n_seg)) / 16 + 1;
   int64_t gx = std::min<int64_t>((cap + n_seg - 1) / n_seg, (per_seg_work + kThreads - 1) / kThreads);
   gx = std::max<int64_t>(gx, 1);
-  dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg));
-  fn<<<grid, kThreads, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? SS_OK : cuda_fail(e);
+  return launch_dependent(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg)), dim3(kThreads), 0, stream, a);
 }
 
 }  // namespace

@@ -179,6 +179,7 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
 template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR>
 __global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
   __shared__ float2 red[2 * (kThreads / 32)];
+  pdl_wait();
   pdl_trigger();  // the slot sum may be scheduled now; it waits for this grid to finish
   const int64_t nvec = (a.n - a.head) / kGroup;
   bool bad = false;
@@ -297,14 +298,14 @@ __global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, fl
 
 template <int MAXR>
 ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
-  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   // One wave: no more blocks than fit on the GPU at once (the kernel's own
   // occupancy), so every block takes the same number of tiles within one and
   // none waits for a free slot while the others finish.
+  ss_status launched = SS_ERR_DTYPE;
   auto go = [&](auto* fn) {
     const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(fn));
     const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min<int64_t>(a.ntiles, cap)));
-    fn<<<grid, kThreads, 0, st>>>(a);
+    launched = launch(fn, grid, a, stream);
   };
   const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
 #define SS_SUMSQ_NR(G, R) \
@@ -338,9 +339,8 @@ ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype 
   }
 #undef SS_SUMSQ_RANKED
 #undef SS_SUMSQ_NR
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
-  return launch_dependent(sum_slots_kernel, 1, kSlotThreads, stream, a.partials, a.ntiles + 1, out);
+  if (launched != SS_OK) return launched;
+  return launch_dependent(sum_slots_kernel, dim3(1), dim3(kSlotThreads), 0, stream, a.partials, a.ntiles + 1, out);
 }
 
 // Shared by ss_grad_sumsq and any entry point that supplies its own slots.
@@ -487,7 +487,8 @@ ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_no
   std::vector<Range> ranges = {rng(shard_sumsq, 8 * static_cast<int64_t>(n_shards), false), rng(coef_out, 4, true)};
   if (norm_out) ranges.push_back(rng(norm_out, 8, true));
   if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
-  return launch_dependent(clip_coef_kernel, 1, 32, stream, shard_sumsq, n_shards, max_norm, coef_out, norm_out);
+  return launch_dependent(clip_coef_kernel, dim3(1), dim3(32), 0, stream, shard_sumsq, n_shards, max_norm, coef_out,
+                          norm_out);
 }
 
 }  // extern "C"

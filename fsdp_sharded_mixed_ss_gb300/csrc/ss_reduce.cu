@@ -19,6 +19,8 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<MAXR>& a, int64_t e,
 
 template <int GT, int MAXR>
 __global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t nvec = (a.n - a.head) / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -53,6 +55,8 @@ __global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_const
 
 template <int GT, int MAXR>
 __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;

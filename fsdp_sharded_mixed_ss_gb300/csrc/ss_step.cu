@@ -33,6 +33,8 @@ __device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float 
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
 __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
@@ -119,6 +121,8 @@ __device__ __forceinline__ void pipe_load(const StepArgs<MAXR>& a, int64_t gi, P
 
 template <int GT, int PT, bool F, bool WRITE_P16, int MAXR, int NR>
 __global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
@@ -178,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_con
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
 __global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  pdl_wait();
+  pdl_trigger();
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -241,6 +247,8 @@ __device__ __forceinline__ void st16_at_phase(void* p, const uint4& v, int phase
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
 __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
+  pdl_wait();
+  pdl_trigger();
   const StepArgs<MAXR>& a = x.s;
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
