@@ -14,6 +14,7 @@ fp32, AdamW on the fp32 master/m/v, cast to 16-bit, unshard copy.
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 from typing import Sequence
@@ -106,6 +107,20 @@ def lib():
 
 # ----------------------------------------------------------------------------- marshalling
 
+_torch = None
+_DTYPES = None
+
+
+def _t():
+    global _torch, _DTYPES
+    if _torch is None:
+        import torch
+
+        _torch = torch
+        _DTYPES = {torch.bfloat16: SS_BF16, torch.float16: SS_FP16, torch.float32: SS_FP32}
+    return _torch
+
+
 def _ptr(x) -> int | None:
     if x is None:
         return None
@@ -115,34 +130,37 @@ def _ptr(x) -> int | None:
 
 
 def _dtype_of(t) -> int | None:
-    import torch
-
     if isinstance(t, int) or t is None:
         return None
-    return {torch.bfloat16: SS_BF16, torch.float16: SS_FP16, torch.float32: SS_FP32}.get(t.dtype)
+    _t()
+    return _DTYPES.get(t.dtype)
 
 
 def _stream(stream, like=None) -> int | None:
     if stream is not None:
         return stream if isinstance(stream, int) else stream.cuda_stream
-    import torch
-
+    torch = _t()
     dev = like.device if (like is not None and not isinstance(like, int) and like.is_cuda) else None
     return torch.cuda.current_stream(dev).cuda_stream
 
 
 class _DeviceGuard:
-    """Makes the tensors' device current for the call (the library sizes grids from it)."""
+    """Makes the tensors' device current for the call (the library sizes grids from it); a no-op
+    when it already is."""
+
+    __slots__ = ("dev", "ctx")
 
     def __init__(self, t):
-        self.dev = t.device if (t is not None and not isinstance(t, int) and t.is_cuda) else None
+        self.dev = None
         self.ctx = None
+        if t is not None and not isinstance(t, int) and t.is_cuda:
+            idx = t.device.index
+            if idx is not None and idx != _t().cuda.current_device():
+                self.dev = idx
 
     def __enter__(self):
         if self.dev is not None:
-            import torch
-
-            self.ctx = torch.cuda.device(self.dev)
+            self.ctx = _torch.cuda.device(self.dev)
             self.ctx.__enter__()
 
     def __exit__(self, *exc):
@@ -155,8 +173,13 @@ def _check(rc: int, where: str) -> None:
         raise SSError(rc, where)
 
 
-def _ptr_array(xs) -> ctypes.Array:
-    return (ctypes.c_void_p * len(xs))(*[_ptr(x) for x in xs])
+def _ptr_array(xs) -> array.array:
+    """The addresses of xs as a C array of 64-bit pointers (keep it alive across the call)."""
+    return array.array("Q", [x if isinstance(x, int) else x.data_ptr() for x in xs])
+
+
+def _addr(a: array.array | None) -> int | None:
+    return a.buffer_info()[0] if a is not None and len(a) else None
 
 
 # ----------------------------------------------------------------------------- layout (host)
@@ -215,7 +238,7 @@ def ss_grad_reduce(rank_grads, n: int, g_out, *, gdtype: int | None = None, post
     gdtype = gdtype if gdtype is not None else _dtype_of(rank_grads[0])
     ptrs = _ptr_array(rank_grads)
     with _DeviceGuard(g_out):
-        _check(_lib.ss_grad_reduce(ctypes.cast(ptrs, ctypes.c_void_p), len(ptrs), -1 if gdtype is None else gdtype,
+        _check(_lib.ss_grad_reduce(_addr(ptrs), len(ptrs), -1 if gdtype is None else gdtype,
                                    n, float(post_scale), int(bool(accumulate)), _ptr(g_out), _ptr(nonfinite_flag),
                                    _stream(stream, g_out)), "ss_grad_reduce")
 
@@ -236,7 +259,7 @@ def ss_adam_step(hp: dict, n: int, master, m, v, *, g32=None, rank_grads=None, g
     ptrs = _ptr_array(ranks) if ranks else None
     opts = _Options(_ptr(g_out), _ptr(nonfinite_flag), _ptr(dev_grad_scale), _ptr(dev_skip_flag))
     with _DeviceGuard(master):
-        _check(_lib.ss_adam_step(ctypes.byref(h), n, _ptr(g32), ctypes.cast(ptrs, ctypes.c_void_p) if ptrs else None,
+        _check(_lib.ss_adam_step(ctypes.byref(h), n, _ptr(g32), _addr(ptrs),
                                  len(ranks), -1 if gdtype is None else gdtype, float(post_scale), _ptr(master), _ptr(m),
                                  _ptr(v), _ptr(param16), -1 if pdtype is None else pdtype, ctypes.byref(opts),
                                  _stream(stream, master)), "ss_adam_step")
@@ -258,7 +281,7 @@ def ss_grad_sumsq(n: int, sumsq_out, workspace, *, g32=None, rank_grads=None, gd
         workspace_bytes = workspace.numel() * workspace.element_size()
     ptrs = _ptr_array(ranks) if ranks else None
     with _DeviceGuard(sumsq_out):
-        _check(_lib.ss_grad_sumsq(n, _ptr(g32), ctypes.cast(ptrs, ctypes.c_void_p) if ptrs else None, len(ranks),
+        _check(_lib.ss_grad_sumsq(n, _ptr(g32), _addr(ptrs), len(ranks),
                                   -1 if gdtype is None else gdtype, float(post_scale), _ptr(sumsq_out),
                                   _ptr(workspace), int(workspace_bytes), _ptr(g_out), _ptr(nonfinite_flag),
                                   _stream(stream, sumsq_out)), "ss_grad_sumsq")
@@ -279,7 +302,7 @@ def ss_grad_sumsq_noalloc(n: int, sumsq_out, *, g32=None, rank_grads=None, gdtyp
         gdtype = _dtype_of(ranks[0])
     ptrs = _ptr_array(ranks) if ranks else None
     with _DeviceGuard(sumsq_out):
-        _check(_lib.ss_grad_sumsq_noalloc(n, _ptr(g32), ctypes.cast(ptrs, ctypes.c_void_p) if ptrs else None,
+        _check(_lib.ss_grad_sumsq_noalloc(n, _ptr(g32), _addr(ptrs),
                                           len(ranks), -1 if gdtype is None else gdtype, float(post_scale),
                                           _ptr(sumsq_out), _ptr(g_out), _ptr(nonfinite_flag),
                                           _stream(stream, sumsq_out)), "ss_grad_sumsq_noalloc")
@@ -298,7 +321,7 @@ def ss_unshard(shards, shard_bounds: np.ndarray, flat, *, dtype: int | None = No
     dtype = dtype if dtype is not None else _dtype_of(flat)
     ptrs = _ptr_array(shards)
     with _DeviceGuard(flat):
-        _check(_lib.ss_unshard(ctypes.cast(ptrs, ctypes.c_void_p), b.ctypes.data, len(ptrs),
+        _check(_lib.ss_unshard(_addr(ptrs), b.ctypes.data, len(ptrs),
                                -1 if dtype is None else dtype, _ptr(flat), _stream(stream, flat)), "ss_unshard")
 
 
@@ -309,4 +332,4 @@ def ss_reshard(flat, shard_bounds: np.ndarray, shards, *, dtype: int | None = No
     ptrs = _ptr_array(shards)
     with _DeviceGuard(flat):
         _check(_lib.ss_reshard(_ptr(flat), b.ctypes.data, len(ptrs), -1 if dtype is None else dtype,
-                               ctypes.cast(ptrs, ctypes.c_void_p), _stream(stream, flat)), "ss_reshard")
+                               _addr(ptrs), _stream(stream, flat)), "ss_reshard")
