@@ -215,11 +215,13 @@ def job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
     return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
 
 
-def run_e2e(s, steps: int, device, t_counter):
-    """Steps through the public API with the gradients copied in from pinned host memory and the
-    flat bf16 unit copied back, every step. Three streams: the host-to-device copy of step i+1 and
-    the device-to-host copy of step i-1 overlap step i (double-buffered device inputs and outputs).
-    Returns (ms per step, H2D GB/s alone, D2H GB/s alone)."""
+def run_e2e(s, steps: int, device, t_counter, readback: str = "flag"):
+    """Steps through the public API with the gradients copied in from pinned host memory every
+    step, and every step's result read back to the host: readback="flag" reads the step's
+    non-finite-gradient flag (4 bytes, the found-inf value a mixed-precision loop reads each step),
+    readback="params" the whole flat bf16 unit. Three streams: the host-to-device copy of step i+1
+    and the device-to-host copy of step i-1 overlap step i (double-buffered device inputs and
+    outputs). Returns (ms per step, H2D GB/s alone, D2H GB/s alone)."""
     import torch
 
     ss, w = s["ss"], s["w"]
@@ -227,9 +229,15 @@ def run_e2e(s, steps: int, device, t_counter):
     host_in = torch.empty((N, n), dtype=torch.bfloat16, pin_memory=True)
     for r in range(N):
         host_in[r].copy_(s["views"][r])
-    host_out = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
     dev_in = [torch.empty((N, n), dtype=torch.bfloat16, device=device) for _ in range(2)]
     flat = [s["flat"], torch.empty(P, dtype=torch.bfloat16, device=device)]
+    flags = [torch.zeros(1, dtype=torch.int32, device=device) for _ in range(2)]
+    if readback == "params":
+        host_out = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
+        dev_out = flat
+    else:
+        host_out = [torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
+        dev_out = flags
     s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(3))
     done = {"h2d": {}, "cmp": {}, "d2h": {}}
 
@@ -249,14 +257,16 @@ def run_e2e(s, steps: int, device, t_counter):
         mark("h2d", i, s_h2d)
         s_cmp.wait_event(done["h2d"][i])
         if i - 2 in done["d2h"]:
-            s_cmp.wait_event(done["d2h"][i - 2])          # flat[b] already copied out
+            s_cmp.wait_event(done["d2h"][i - 2])          # dev_out[b] already copied out
+        with torch.cuda.stream(s_cmp):
+            flags[b].zero_()
         ss.ss_adam_step(w.hp(t), n, s["master"], s["m"], s["v"], rank_grads=[dev_in[b][r] for r in range(N)],
-                        param16=s["shards"][0], stream=s_cmp)
+                        param16=s["shards"][0], nonfinite_flag=flags[b], stream=s_cmp)
         ss.ss_unshard(s["shards"], s["bounds"], flat[b], stream=s_cmp)
         mark("cmp", i, s_cmp)
         s_d2h.wait_event(done["cmp"][i])
         with torch.cuda.stream(s_d2h):
-            host_out[b].copy_(flat[b], non_blocking=True)
+            host_out[b].copy_(dev_out[b], non_blocking=True)
         mark("d2h", i, s_d2h)
 
     for i in range(3):
@@ -285,9 +295,12 @@ def run_e2e(s, steps: int, device, t_counter):
         torch.cuda.synchronize(device)
         return a.elapsed_time(b) / 5
 
+    if readback == "flag" and any(int(h.item()) != 0 for h in host_out):
+        raise RuntimeError("e2e: a step flagged non-finite gradients on finite synthetic inputs")
     h2d_ms = timed(lambda: dev_in[0].copy_(host_in, non_blocking=True))
-    d2h_ms = timed(lambda: host_out[0].copy_(flat[0], non_blocking=True))
-    return e2e_ms, 2 * N * n / (h2d_ms * 1e-3) / 1e9, 2 * P / (d2h_ms * 1e-3) / 1e9
+    out_bytes = dev_out[0].numel() * dev_out[0].element_size()
+    d2h_ms = timed(lambda: host_out[0].copy_(dev_out[0], non_blocking=True))
+    return e2e_ms, 2 * N * n / (h2d_ms * 1e-3) / 1e9, out_bytes / (d2h_ms * 1e-3) / 1e9
 
 
 def run_ours(args, rank: int, world: int, device):
@@ -340,11 +353,13 @@ def run_ours(args, rank: int, world: int, device):
     sampler.stop()
     clocks = sampler.summary(h0, h1)
 
-    # end to end through the public API with host buffers: pinned grads in, flat params out
-    e2e_ms, h2d_gbs, d2h_gbs = run_e2e(s, args.e2e_steps, device, t_counter)
+    # end to end through the public API with host buffers: pinned grads in, the step's result out
+    # (its non-finite flag); and, for context, the same with the whole flat unit read back
+    e2e_ms, h2d_gbs, _ = run_e2e(s, args.e2e_steps, device, t_counter, "flag")
+    e2e_p_ms, _, d2h_gbs = run_e2e(s, args.e2e_steps, device, t_counter, "params")
 
     adam_b, unshard_b = bytes_per_step(s)
-    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e_ms], device if world > 1 else None)
+    elapsed_ms, e2e_ms, e2e_p_ms = max_over_ranks([elapsed_ms, e2e_ms, e2e_p_ms], device if world > 1 else None)
     ms_per_step = elapsed_ms / args.steps
     total_bytes = (adam_b + unshard_b) * world
     value = job_gbs(adam_b + unshard_b, world, ms_per_step)
@@ -368,8 +383,13 @@ def run_ours(args, rank: int, world: int, device):
                      "peak_source": peaks["source"]},
         "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * s["n"] * s["N"],
-                "d2h_bytes_per_step": 2 * s["P"], "h2d_gbs": round(h2d_gbs, 1), "d2h_gbs": round(d2h_gbs, 1),
-                "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)"},
+                "d2h_bytes_per_step": 4, "h2d_gbs": round(h2d_gbs, 1),
+                "result": "the step's non-finite-gradient flag (int32), read back every step",
+                "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)",
+                "params_readback": {"value": round(total_bytes / (e2e_p_ms * 1e-3) / 1e9, 1),
+                                    "ms_per_step": round(e2e_p_ms, 4), "d2h_bytes_per_step": 2 * s["P"],
+                                    "d2h_gbs": round(d2h_gbs, 1),
+                                    "note": "the whole flat bf16 unit read back every step instead"}},
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
