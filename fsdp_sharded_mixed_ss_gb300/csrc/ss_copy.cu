@@ -161,18 +161,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-// Wait for the phase of the given parity to complete, for at most ~1 s.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of the given parity to complete, for at most limit_ns
+// (~1 s by default); on expiry set the timeout bit of the device error word
+// and return false.
+__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       atomicOr(&g_device_error, SS_DEVERR_TIMEOUT);
       return false;
     }
   }
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// arrives at, so the wait runs out after limit_ns and reports through the
+// device error word, exactly as a bulk-copy wait would. Nothing is in flight
+// on the barrier, so the block simply returns.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint64_t limit_ns) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  const uint32_t b = smem_addr(&bar);
+  mbar_init(b, 1u);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_wait(b, 0u, limit_ns);
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -310,6 +327,12 @@ ss_status run_copy(const void* const* src, void* const* dst, const int64_t* byte
 using namespace ss;
 
 extern "C" {
+
+ss_status ss_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000000 || limit_ns > 2000000000) return SS_ERR_INVALID_ARG;
+  return launch_dependent(wait_timeout_selftest_kernel, dim3(1), dim3(32), 0, stream,
+                          static_cast<uint64_t>(limit_ns));
+}
 
 ss_status ss_device_error(uint32_t* out, int32_t clear) {
   if (!out) return SS_ERR_INVALID_ARG;

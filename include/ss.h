@@ -259,6 +259,15 @@ const char* ss_last_cuda_error(void);           /* last CUDA error text of this 
  * to *out (host) and, when clear != 0, resets it. Synchronous: it waits for
  * the work already queued on the device. */
 ss_status ss_device_error(uint32_t* out, int32_t clear);
+
+/* Self-test of the bounded-wait path (no counterpart on the pages): launches,
+ * on `stream`, one block that waits on a shared-memory barrier nothing ever
+ * completes, using the same bounded wait as the bulk-copy kernel but with a
+ * limit of limit_ns nanoseconds (1e6 .. 2e9, else SS_ERR_INVALID_ARG and
+ * nothing is launched). The wait runs out, sets bit 0 of the device error
+ * word and the block returns; the context stays usable. For testing failure
+ * reporting without a fault: clear the word afterwards. */
+ss_status ss_selftest_wait_timeout(int64_t limit_ns, void* stream);
 int32_t ss_abi_version(void);                   /* SS_ABI_VERSION */
 
 #ifdef __cplusplus

@@ -156,6 +156,14 @@ def test_sumsq_and_clip_argument_errors(ss):
     assert e.value.status == 3
 
 
+def test_wait_selftest_limit_checked_on_host(ss):
+    # the bounded-wait self-test only accepts limits of 1 ms .. 2 s, and says so before any launch
+    for bad in (0, 999_999, 2_000_000_001, -5):
+        with pytest.raises(ss.SSError) as e:
+            ss.ss_selftest_wait_timeout(bad, stream=0)
+        assert e.value.status == 1
+
+
 def test_noalloc_size_limit_rejected_on_host(ss):
     # n above the fixed scratch capacity is refused before anything touches a GPU
     with pytest.raises(ss.SSError) as e:
