@@ -320,6 +320,127 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
   }
 }
 
+// Warp-cooperative, register double-buffered form of the shifted-load step for
+// up to 8 16-bit rank gradients that all sit at the same 16-byte phase (views
+// at one offset into identically allocated buffers, the usual case). A warp
+// takes runs of 31 consecutive groups of the vector body: lane j loads, per
+// rank, the aligned 16-byte chunk under the start of group j of the run (lane
+// 31 the chunk under the start of the group after the run) and sums the
+// ranks' chunks element by element in rank order -- the same fp32 sum each
+// element gets anywhere else, only held in a neighbouring register -- then
+// lanes 0..30 take the upper lane's 8 sums with shuffles and pick their
+// group's 8 out of the 16. Each gradient byte is loaded once; lanes 0..30
+// load their group's state; the loads of the warp's next run are issued
+// before the current run's update, as in the aligned double-buffered kernel.
+// Every chunk lies under a group in [1, nvec - 1], so inside its array; the
+// groups outside the body [1, nvec - 1) and the head/tail elements are done
+// one by one.
+constexpr int kRun = 31;  // groups per warp run
+
+template <int GT, int NR, int MAXR>
+__device__ __forceinline__ void shift_pipe_load(const ShiftArgs<MAXR>& x, int64_t run, int lane, int64_t nvec,
+                                                PipeGroup<NR>& G) {
+  const StepArgs<MAXR>& a = x.s;
+  int64_t gi = 1 + run * kRun + lane;  // the group whose start this lane's chunks cover
+  gi = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the array, unused
+  const int64_t e = a.head + gi * kGroup;
+#pragma unroll
+  for (int r = 0; r < NR; ++r)
+    G.r[r] = __ldcs(reinterpret_cast<const uint4*>(
+        reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e) - x.rphase[0]));
+  if (lane < kRun) {
+    const int64_t gb = gi < nvec - 2 ? gi : nvec - 2;  // the state of a body group
+    const int64_t es = a.head + gb * kGroup;
+    G.s[0] = __ldcs(reinterpret_cast<const float4*>(a.master + es));
+    G.s[1] = __ldcs(reinterpret_cast<const float4*>(a.master + es) + 1);
+    G.s[2] = __ldcs(reinterpret_cast<const float4*>(a.m + es));
+    G.s[3] = __ldcs(reinterpret_cast<const float4*>(a.m + es) + 1);
+    G.s[4] = __ldcs(reinterpret_cast<const float4*>(a.v + es));
+    G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + es) + 1);
+  }
+}
+
+// g[i] = element SH + i of the 16 values (c, d).
+template <int SH>
+__device__ __forceinline__ void take8(const float (&c)[8], const float (&d)[8], float (&g)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = SH + i < 8 ? c[SH + i] : d[SH + i - 8];
+}
+
+template <int GT, int PT, bool WRITE_P16, int MAXR, int NR>
+__global__ void __launch_bounds__(kThreads, 2) adam_shift_pipe_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
+  pdl_wait();
+  pdl_trigger();
+  const StepArgs<MAXR>& a = x.s;
+  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
+  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
+  const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
+  const int64_t nbody = nvec - 2;                 // groups 1 .. nvec - 2
+  const int64_t runs = (nbody + kRun - 1) / kRun;
+  const int sh = x.rphase[0] >> 1;                // the groups' element offset into their first chunk
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  bool bad = false;
+  PipeGroup<NR> cur, nxt;
+  if (warp < runs) shift_pipe_load<GT, NR>(x, warp, lane, nvec, cur);
+  for (int64_t run = warp; run < runs; run += nwarps) {  // warp-uniform
+    if (run + nwarps < runs) shift_pipe_load<GT, NR>(x, run + nwarps, lane, nvec, nxt);
+    float c[8], d[8], g[8];
+    widen8<GT>(cur.r[0], c);
+#pragma unroll
+    for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], c);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = __shfl_down_sync(0xFFFFFFFFu, c[i], 1);
+    switch (sh) {
+      case 0: take8<0>(c, d, g); break;
+      case 1: take8<1>(c, d, g); break;
+      case 2: take8<2>(c, d, g); break;
+      case 3: take8<3>(c, d, g); break;
+      case 4: take8<4>(c, d, g); break;
+      case 5: take8<5>(c, d, g); break;
+      case 6: take8<6>(c, d, g); break;
+      default: take8<7>(c, d, g); break;
+    }
+    const int64_t gi = 1 + run * kRun + lane;
+    if (lane < kRun && gi < nvec - 1) {
+      const int64_t e = a.head + gi * kGroup;
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+      if (a.nonfinite) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+      }
+      if (a.g_out) st8f(a.g_out + e, g);
+      if (a.dev_scale) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+      }
+      float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
+      float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
+      float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+      st8f(a.master + e, p);
+      st8f(a.m + e, m);
+      st8f(a.v + e, v);
+      if constexpr (WRITE_P16) st16_at_phase(static_cast<uint16_t*>(a.p16) + e, narrow8<PT>(p), x.pphase);
+    }
+    cur = nxt;
+  }
+  // everything outside the vector body, one element per thread (< 31 elements)
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t lo_end = a.head + kGroup, hi_start = a.head + (nvec - 1) * kGroup;
+  const int64_t n_edge = lo_end + (a.n - hi_start);
+  if (tid < n_edge) step1<GT, PT, false, WRITE_P16>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), gs, bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
+  }
+}
+
 // Splits a double into an fp32 pair hi + lo (hi = nearest float, lo = nearest float to the rest).
 void split(double x, float& hi, float& lo) {
   hi = static_cast<float>(x);
@@ -354,6 +475,13 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 enum class Path { kScalar, kVector, kPipe, kShift };
 
+template <int G, int P, bool W, int MAXR, int NR>
+ss_status launch_shift_pipe_n(const ShiftArgs<MAXR>& x, void* stream) {
+  auto* fn = adam_shift_pipe_kernel<G, P, W, MAXR, NR>;
+  const int64_t runs = ((x.s.n - x.s.head) / kGroup - 2 + kRun - 1) / kRun;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32), x, stream);
+}
+
 template <int G, int P, bool F, bool W, int MAXR>
 ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t pphase, void* stream) {
   ShiftArgs<MAXR> x;
@@ -361,6 +489,22 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
   x.s = a;
   for (int32_t r = 0; r < a.n_ranks; ++r) x.rphase[r] = rphase[r];
   x.pphase = pphase;
+  // up to 8 16-bit gradients at one phase: the warp-cooperative double-buffered form
+  bool same = true;
+  for (int32_t r = 1; r < a.n_ranks; ++r) same = same && rphase[r] == rphase[0];
+  if constexpr (!F && MAXR == kSmallRanks) {
+    if (same) switch (a.n_ranks) {
+      case 1: return launch_shift_pipe_n<G, P, W, MAXR, 1>(x, stream);
+      case 2: return launch_shift_pipe_n<G, P, W, MAXR, 2>(x, stream);
+      case 3: return launch_shift_pipe_n<G, P, W, MAXR, 3>(x, stream);
+      case 4: return launch_shift_pipe_n<G, P, W, MAXR, 4>(x, stream);
+      case 5: return launch_shift_pipe_n<G, P, W, MAXR, 5>(x, stream);
+      case 6: return launch_shift_pipe_n<G, P, W, MAXR, 6>(x, stream);
+      case 7: return launch_shift_pipe_n<G, P, W, MAXR, 7>(x, stream);
+      case 8: return launch_shift_pipe_n<G, P, W, MAXR, 8>(x, stream);
+      default: break;
+    }
+  }
   auto* fn = adam_shift_kernel<G, P, F, W, MAXR>;
   return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), x, stream);
 }

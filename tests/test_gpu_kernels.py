@@ -281,6 +281,32 @@ def test_step_split_calls_agree(ss):
     assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
 
 
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("n", [27, 40, 1000, 300_007])
+@pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
+@pytest.mark.parametrize("same", [True, False])
+def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
+    """Rank views off the aligned state's phase: all at one offset (1..7, the warp-cooperative
+    kernel for N <= 8) or rank r at (r % 7) + 1 (mixed phases: the per-thread kernel), from a
+    1-group body (n = 27) to many runs per warp; equal to the aligned kernel bit for bit and to
+    the oracle."""
+    import torch
+    hp = dict(HP, step=5)
+    ref = _oracle_step(n, N, fmt, hp)
+    G_al = [dev_bits(s, n) for s in ref[0]]
+    offs = [(n % 7) + 1] * N if same else [(r % 7) + 1 for r in range(N)]
+    G_off = [dev_bits(s, n, offset=o) for s, o in zip(ref[0], offs)]
+    a, b = _state(n), _state(n)
+    pa = torch.zeros(n, dtype=tdt(fmt), device="cuda")
+    pb = torch.zeros(n + 2, dtype=tdt(fmt), device="cuda")[(n % 3):(n % 3) + n]
+    ss.ss_adam_step(hp, n, *a, rank_grads=G_al, param16=pa)
+    ss.ss_adam_step(hp, n, *b, rank_grads=G_off, param16=pb)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+    _check(*b, pb, ref, fmt)
+
+
 @pytest.mark.parametrize("goffs,poff", [((1,) * 8, 0), ((0, 1, 2, 3, 4, 5, 6, 7), 3), ((3,) * 8, 1)])
 def test_step_views_off_phase_match_aligned(ss, goffs, poff):
     """Rank views (and param16) off the state's 16-byte phase take the shifted-load kernel;
