@@ -185,3 +185,35 @@ def test_library_call_right_after_a_torch_kernel(ss):
         ref = oracle.grad_reduce([synth.host_range(synth.normal(1e-3, synth.FP16, synth.GRAD, r, i + 1), 0, n)
                                   for r in range(N)], oracle.FP16)
         assert np.array_equal(outs[i].cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_library_call_right_after_a_host_copy_and_across_streams(ss):
+    """Each kernel waits for whatever precedes it in its stream, not only kernels: gradients
+    copied in from pinned host memory right before the reduce (same stream), and copied on a
+    second stream that the reduce's stream waits for through an event, eight times each with
+    different contents: every result equals the oracle's sum of the copied values."""
+    import torch
+    n, N = 1_500_007, 2
+    specs = [[synth.normal(1e-3, synth.BF16, synth.GRAD, r, i + 1) for r in range(N)] for i in range(8)]
+    host = [[torch.from_numpy(synth.host_range(s, 0, n).view(np.int16)).pin_memory() for s in row] for row in specs]
+    G = [torch.empty(n, dtype=torch.bfloat16, device="cuda") for _ in range(N)]
+    outs = [torch.empty(n, device="cuda") for _ in range(16)]
+    copy_stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for i in range(8):                                   # same stream: copy, then reduce
+        for r in range(N):
+            G[r].view(torch.int16).copy_(host[i][r], non_blocking=True)
+        ss.ss_grad_reduce(G, n, outs[i])
+    for i in range(8):                                   # copy on another stream, event, reduce
+        copy_stream.wait_stream(torch.cuda.current_stream())   # G no longer read by the last reduce
+        with torch.cuda.stream(copy_stream):
+            for r in range(N):
+                G[r].view(torch.int16).copy_(host[i][r], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(copy_stream)
+        torch.cuda.current_stream().wait_event(ev)
+        ss.ss_grad_reduce(G, n, outs[8 + i])
+    torch.cuda.synchronize()
+    for j in range(16):
+        ref = oracle.grad_reduce([synth.host_range(s, 0, n) for s in specs[j % 8]], oracle.BF16)
+        assert np.array_equal(outs[j].cpu().numpy().view(np.uint32), ref.view(np.uint32))
