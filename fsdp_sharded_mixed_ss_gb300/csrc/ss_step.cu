@@ -94,6 +94,10 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
 #ifndef SS_PIPE_MAX_RANKS
 #define SS_PIPE_MAX_RANKS 8
 #endif
+// Rank counts up to which the kernel also prefetches into L2 (measured on
+// GB300: +2-6% for an fp32 gradient and N <= 4, -5% at N = 8, where a group's
+// own loads already keep enough bytes in flight).
+constexpr int kPipePrefetchRanks = 4;
 template <int NR>
 struct PipeGroup {
   uint4 r[NR];
@@ -131,8 +135,35 @@ __global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_con
   bool bad = false;
   PipeGroup<NR> cur, nxt;
   if (tid < nvec) pipe_load<GT, NR, F>(a, tid, cur);
+  const int lane = threadIdx.x & 31;
   for (int64_t gi = tid; gi < nvec; gi += stride) {
     if (gi + stride < nvec) pipe_load<GT, NR, F>(a, gi + stride, nxt);
+    if constexpr (F || NR <= kPipePrefetchRanks) {
+      // L2 prefetch of the warp's groups two iterations ahead, one bulk prefetch per array
+      // (lane k takes array k): more bytes in flight without registers, for groups whose own
+      // loads are few. Hints only; every range lies inside its array.
+      constexpr int kArrays = (F ? 1 : NR) + 3;
+      const int64_t b = (gi - lane) + 2 * stride;
+      if (b < nvec && lane < kArrays) {
+        const int64_t cnt = nvec - b < 32 ? nvec - b : 32;
+        const int64_t e = a.head + b * kGroup;
+        const char* base;
+        int64_t bytes = cnt * 32;  // 8 fp32 per group
+        if (lane < kArrays - 3) {
+          if constexpr (F) {
+            base = reinterpret_cast<const char*>(a.g32 + e);
+          } else {
+            base = reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[lane]) + e);
+            bytes = cnt * 16;  // 8 16-bit per group
+          }
+        } else {
+          const int k = lane - (kArrays - 3);
+          base = reinterpret_cast<const char*>((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + e);
+        }
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base), "r"(static_cast<uint32_t>(bytes))
+                     : "memory");
+      }
+    }
     const int64_t e = a.head + gi * kGroup;
     float g[8];
     if constexpr (F) {
