@@ -129,6 +129,12 @@ __device__ __forceinline__ void st8f(float* p, const float (&f)[8]) {
 
 __device__ __forceinline__ bool finite(float x) { return fabsf(x) <= 3.402823466e38f; }
 
+// Hint to the L2: fetch `bytes` bytes at p from DRAM now (one bulk prefetch;
+// p 16-byte aligned, bytes a multiple of 16, the range inside one array).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ------------------------------------------------------------------ argument blocks
 
 template <int MAXR>

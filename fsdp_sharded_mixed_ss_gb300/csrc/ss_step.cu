@@ -160,8 +160,7 @@ __global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_con
           const int k = lane - (kArrays - 3);
           base = reinterpret_cast<const char*>((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + e);
         }
-        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(base), "r"(static_cast<uint32_t>(bytes))
-                     : "memory");
+        prefetch_l2(base, static_cast<uint32_t>(bytes));
       }
     }
     const int64_t e = a.head + gi * kGroup;
