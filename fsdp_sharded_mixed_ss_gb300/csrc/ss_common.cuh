@@ -243,7 +243,8 @@ Range rng(const void* p, int64_t bytes, bool out);
 // elements and every fp32 pointer likewise; -1 when none exists.
 int common_phase(const std::vector<uintptr_t>& p16, const std::vector<uintptr_t>& p32);
 int sm_count();
-// Resident blocks per SM of a kernel launched with `threads` per block (cached per kernel).
+// Resident blocks per SM of a kernel launched with `threads` per block (cached per device,
+// kernel and block size).
 int blocks_per_sm(const void* fn, int threads = kThreads);
 // Persistent grid for `work_items` thread-items: at most SM count x resident blocks.
 unsigned grid_for(const void* fn, int64_t work_items, int threads = kThreads);

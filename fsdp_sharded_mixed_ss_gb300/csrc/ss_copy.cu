@@ -272,16 +272,23 @@ __global__ void __launch_bounds__(32) copy_tma_kernel(const __grid_constant__ Co
     mbar_wait(bar0 + 8u * static_cast<uint32_t>(j % kTmaSlots), static_cast<uint32_t>((j / kTmaSlots) & 1));
 }
 
-// Raise a kernel's dynamic shared memory limit once (cached per kernel).
+// Raise a kernel's dynamic shared memory limit once per device (cached per device and kernel).
 bool allow_smem(const void* fn, size_t bytes) {
+  struct Done {
+    int dev;
+    const void* fn;
+    size_t bytes;
+  };
   static std::mutex mu;
-  static std::vector<std::pair<const void*, size_t>> done;
+  static std::vector<Done> done;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
   std::lock_guard<std::mutex> lock(mu);
-  for (auto& d : done)
-    if (d.first == fn && d.second >= bytes) return true;
+  for (const Done& d : done)
+    if (d.dev == dev && d.fn == fn && d.bytes >= bytes) return true;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
     return false;
-  done.emplace_back(fn, bytes);
+  done.push_back({dev, fn, bytes});
   return true;
 }
 

@@ -48,14 +48,21 @@ int sm_count() {
 }
 
 int blocks_per_sm(const void* fn, int threads) {
+  struct Entry {
+    int dev;
+    const void* fn;
+    int threads, blocks;
+  };
   static std::mutex mu;
-  static std::vector<std::pair<const void*, int>> cache;
+  static std::vector<Entry> cache;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   std::lock_guard<std::mutex> lock(mu);
-  for (auto& c : cache)
-    if (c.first == fn) return c.second;
+  for (const Entry& c : cache)
+    if (c.dev == dev && c.fn == fn && c.threads == threads) return c.blocks;
   int b = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, 0) != cudaSuccess || b < 1) b = 1;
-  cache.emplace_back(fn, b);
+  cache.push_back({dev, fn, threads, b});
   return b;
 }
 

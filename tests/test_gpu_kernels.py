@@ -157,6 +157,36 @@ def test_step_rank_counts(ss, N, fmt):
     _check(master, m, v, p16, ref, fmt)
 
 
+@pytest.mark.parametrize("gfmt,pfmt", [(synth.BF16, synth.FP16), (synth.FP16, synth.BF16), (synth.BF16, synth.BF16),
+                                       (synth.FP16, synth.FP16), (synth.FP32, synth.FP16), (synth.FP32, synth.BF16)])
+@pytest.mark.parametrize("N,goff", [(3, 0), (9, 0), (3, 5)])
+def test_step_gradient_and_param_formats(ss, gfmt, pfmt, N, goff):
+    """Every pairing of gradient format (bf16, fp16, or an fp32 gradient) with parameter format,
+    through the double-buffered (N = 3), single-buffered (N = 9) and shifted-load (views 5
+    elements off) kernels, against the oracle."""
+    import torch
+    n = 30_011
+    hp = dict(HP, step=7)
+    master0 = host_bits(synth.normal(0.02, synth.FP32, synth.MASTER), n).view(np.float32).copy()
+    m0 = host_bits(synth.normal(1e-4, synth.FP32, synth.MOM1), n).view(np.float32).copy()
+    v0 = host_bits(synth.normal(1e-8, synth.FP32, synth.MOM2, absolute=True), n).view(np.float32).copy()
+    master, m, v = _state(n)
+    p16 = torch.zeros(n, dtype=tdt(pfmt), device="cuda")
+    if gfmt == synth.FP32:
+        spec = synth.normal(1e-3, synth.FP32, synth.GRAD, 0, 7)
+        g = host_bits(spec, n).view(np.float32).copy()
+        g32 = dev_bits(spec, n, offset=goff)   # off by 5: no common phase with the state, element-wise
+        ss.ss_adam_step(hp, n, master, m, v, g32=g32, param16=p16)
+    else:
+        specs = [synth.normal(1e-3, gfmt, synth.GRAD, r, 7) for r in range(N)]
+        g = oracle.grad_reduce([host_bits(s_, n) for s_ in specs], gfmt)
+        G = [dev_bits(s_, n, offset=goff) for s_ in specs]
+        ss.ss_adam_step(hp, n, master, m, v, rank_grads=G, param16=p16)
+    rp = oracle.adamw(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], hp["step"], g, master0, m0,
+                      v0, p16_dtype=pfmt)
+    _check(master, m, v, p16, (None, g, master0, m0, v0, rp), pfmt)
+
+
 def test_step_from_fp32_grad_matches_fused(ss):
     import torch
     n, N = 50_001, 8
