@@ -1,9 +1,11 @@
 // ss_step.cu -- the fused shard step (ss_adam_step): rank-ordered fp32 reduce of
 // the ranks' gradient shards, AdamW on the fp32 master and moments, and the
-// 16-bit parameter cast, in one pass over HBM. Four kernel forms share the
+// 16-bit parameter cast, in one pass over HBM. Five kernel forms share the
 // per-element arithmetic of ss_math.cuh: register double-buffered (up to 8
-// ranks or an fp32 gradient), single-buffered vector (more ranks), shifted
-// loads (16-bit arrays off the state's 16-byte phase) and element-wise.
+// ranks or an fp32 gradient), single-buffered vector (more ranks), two with
+// shifted loads for 16-bit arrays off the state's 16-byte phase (a
+// warp-cooperative double-buffered one for up to 8 ranks at one phase, a
+// per-thread one otherwise) and element-wise.
 #include "ss_common.cuh"
 
 namespace ss {
@@ -234,9 +236,9 @@ __global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_cons
 // boundary -- groups still start where the fp32 arrays are 16-byte aligned.
 // Every 16-bit gradient array is read as the two aligned 16-byte chunks that
 // hold the group (all loads issued first) and funnel-shifted to its phase;
-// param16 is stored in 4- or 2-byte pieces when it is off phase. The body is groups 1 .. nvec-2, so every chunk read lies inside its
-// array; the first and last groups and the head/tail elements are done one by
-// one.
+// param16 is stored in 4- or 2-byte pieces when it is off phase. The body is
+// groups 1 .. nvec-2, so every chunk read lies inside its array; the first
+// and last groups and the head/tail elements are done one by one.
 template <int MAXR>
 struct ShiftArgs {
   StepArgs<MAXR> s;
