@@ -448,12 +448,27 @@ def run_suite(args, device) -> dict:
         out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
         out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
         if N == 8:
-            # gradient views one element off the state's 16-byte phase: the element-wise path
+            # gradient views one element off the state's 16-byte phase: the shifted-load kernels
             Gm = [g[1:] for g in G]
             m1 = n - 1
             out["adam_step_N8_grads_off_by_one"] = entry(
                 timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1]), 5),
                 (2 * N + 26) * m1)
+            # next rows: gradient accumulation (read-modify-write of the fp32 gradient) ...
+            out["grad_reduce_accumulate_N8"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32, accumulate=True)),
+                                                     (2 * N + 8) * n)
+            # ... fp16 loss-scale unscaling with the overflow flag and the skip flag read ...
+            G16 = [g.view(torch.float16) for g in G]   # the same bits read as fp16: finite, small
+            flag = torch.zeros(2, dtype=torch.int32, device=device)   # [0]: this step's flag, [1]: skip
+            out["adam_step_N8_fp16_unscale_flag_skip"] = entry(
+                timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G16, post_scale=1.0 / 1024, param16=p16,
+                                              nonfinite_flag=flag[0:1], dev_skip_flag=flag[1:2])), (2 * N + 26) * n)
+            assert int(flag[0].item()) == 0
+            # ... and the 16-bit parameters written straight into a flat unit buffer at the shard's offset
+            flat = torch.empty(n + 1024, dtype=torch.bfloat16, device=device)
+            out["adam_step_N8_param16_into_flat"] = entry(
+                timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=flat[1024:])), (2 * N + 26) * n)
+            del flat, flag
         del G
         torch.cuda.empty_cache()
     del st, p16, g32, ws
