@@ -144,13 +144,15 @@ def test_step_odd_lengths_and_views(ss, n, goff, soff, poff):
     _check(master, m, v, p16, ref, fmt)
 
 
-@pytest.mark.parametrize("N", [1, 2, 9, 64, 130])
+@pytest.mark.parametrize("N,goff", [(1, 0), (2, 0), (9, 0), (64, 0), (130, 0), (1024, 0), (1024, 3), (65, 1)])
 @pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
-def test_step_rank_counts(ss, N, fmt):
+def test_step_rank_counts(ss, N, goff, fmt):
+    """Rank counts across the kernel forms and both pointer-table sizes, up to the maximum 1024
+    (aligned, and all views off the state's phase: the per-thread shifted kernel)."""
     import torch
     n = 20_011
     ref = _oracle_step(n, N, fmt, HP)
-    G = [dev_bits(s, n) for s in ref[0]]
+    G = [dev_bits(s, n, offset=goff) for s in ref[0]]
     master, m, v = _state(n)
     p16 = torch.zeros(n, dtype=tdt(fmt), device="cuda")
     ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16)
