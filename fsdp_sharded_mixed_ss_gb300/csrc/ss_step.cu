@@ -33,6 +33,14 @@ __device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float 
   if constexpr (WRITE_P16) static_cast<uint16_t*>(a.p16)[e] = narrow1<PT>(p);
 }
 
+// Rank counts up to which the single-buffered kernel also prefetches its
+// warp's next groups into L2 (measured on GB300 at 2^26 elements: +7-12% for
+// N = 9-12, -4.5% at N = 16).
+#ifndef SS_VEC_PF_RANKS
+#define SS_VEC_PF_RANKS 12
+#endif
+constexpr int kVecPrefetchRanks = SS_VEC_PF_RANKS;
+
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
 __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
   pdl_wait();
@@ -43,8 +51,25 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
+  // moderate rank counts: the warp also asks the L2 for its next groups, one bulk prefetch per
+  // array (lane k takes array k), as the double-buffered kernel does for few ranks
+  const int lane = threadIdx.x & 31;
+  const int npf = (!FROM_G32 && a.n_ranks <= kVecPrefetchRanks) ? a.n_ranks + 3 : 0;
   for (int64_t gi = tid; gi < nvec; gi += stride) {
     const int64_t e = a.head + gi * kGroup;
+    if (npf) {
+      const int64_t b = (gi - lane) + stride;
+      if (b < nvec && lane < npf) {
+        const int64_t cnt = nvec - b < 32 ? nvec - b : 32;
+        const int64_t eb = a.head + b * kGroup;
+        if (lane < a.n_ranks) {
+          prefetch_l2(static_cast<const uint16_t*>(a.ranks.p[lane]) + eb, static_cast<uint32_t>(cnt * 16));
+        } else {
+          const int k = lane - a.n_ranks;
+          prefetch_l2((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + eb, static_cast<uint32_t>(cnt * 32));
+        }
+      }
+    }
     float g[8];
     if constexpr (FROM_G32) {
       ld8f(a.g32 + e, g);
@@ -97,9 +122,12 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
 #define SS_PIPE_MAX_RANKS 8
 #endif
 // Rank counts up to which the kernel also prefetches into L2 (measured on
-// GB300: +2-6% for an fp32 gradient and N <= 4, -5% at N = 8, where a group's
-// own loads already keep enough bytes in flight).
-constexpr int kPipePrefetchRanks = 4;
+// GB300 at 2^26 elements: +2-9% for an fp32 gradient and N <= 6, -5% at N = 8,
+// where a group's own loads already keep enough bytes in flight).
+#ifndef SS_PIPE_PF_RANKS
+#define SS_PIPE_PF_RANKS 6
+#endif
+constexpr int kPipePrefetchRanks = SS_PIPE_PF_RANKS;
 template <int NR>
 struct PipeGroup {
   uint4 r[NR];
