@@ -471,6 +471,19 @@ def run_suite(args, device) -> dict:
             del flat, flag
         del G
         torch.cuda.empty_cache()
+    # the fused step across the rank counts between (kernel forms and prefetch thresholds)
+    G = []
+    for r in range(32):
+        t = torch.empty(n, dtype=torch.bfloat16, device=device)
+        synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+        G.append(t)
+    by_ranks = {}
+    for N in (1, 3, 4, 5, 6, 7, 9, 10, 12, 13, 16, 24, 32):
+        Gn = G[:N]
+        by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=Gn, param16=p16)),
+                                 (2 * N + 26) * n)
+    out["adam_step_by_ranks"] = by_ranks
+    del G
     del st, p16, g32, ws
     torch.cuda.empty_cache()
     for name, numels, N, dt in (("unshard_gpt2_small_N8", [124_439_808], 8, torch.bfloat16),
