@@ -114,13 +114,18 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
 
 // Register double-buffered form for small rank counts: the loads of a
 // thread's next group are issued before the update of its current group, so
-// each thread keeps two groups of bytes in flight (for N <= SS_PIPE_MAX_RANKS,
-// where one group alone is too few bytes to cover HBM latency at the
+// each thread keeps two groups of bytes in flight (for small N, where one
+// group alone is too few bytes to cover HBM latency at the
 // residency the update's registers allow). NR is the rank count; with F the
 // gradient is the fp32 array g32, held as NR = 2 raw 16-byte chunks.
-#ifndef SS_PIPE_MAX_RANKS
-#define SS_PIPE_MAX_RANKS 8
+// The rank counts (bit N set: N ranks) that take this form; the others take
+// the single-buffered kernel, which with its L2 prefetch measured faster on
+// GB300 for 5 and 6 ranks at 2^26 elements.
+#ifndef SS_PIPE_RANK_MASK
+#define SS_PIPE_RANK_MASK ((1u << 1) | (1u << 2) | (1u << 3) | (1u << 4) | (1u << 7) | (1u << 8))
 #endif
+constexpr unsigned kPipeRankMask = SS_PIPE_RANK_MASK;
+constexpr bool pipe_ranks(int n) { return n >= 1 && n <= 8 && ((kPipeRankMask >> n) & 1u) != 0; }
 // Rank counts up to which the kernel also prefetches into L2 (measured on
 // GB300 at 2^26 elements: +2-9% for an fp32 gradient and N <= 6, -5% at N = 8,
 // where a group's own loads already keep enough bytes in flight).
@@ -577,23 +582,16 @@ ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
 
 template <int G, int P, bool W, int MAXR>
 ss_status launch_pipe(const StepArgs<MAXR>& a, void* stream) {
+#define SS_PIPE_CASE(R)                                                     \
+  case R:                                                                   \
+    if constexpr (pipe_ranks(R)) return launch_pipe_n<G, P, W, MAXR, R>(a, stream); \
+    else return SS_ERR_INVALID_ARG;
   switch (a.n_ranks) {
-    case 1: return launch_pipe_n<G, P, W, MAXR, 1>(a, stream);
-    case 2: return launch_pipe_n<G, P, W, MAXR, 2>(a, stream);
-#if SS_PIPE_MAX_RANKS >= 3
-    case 3: return launch_pipe_n<G, P, W, MAXR, 3>(a, stream);
-#endif
-#if SS_PIPE_MAX_RANKS >= 4
-    case 4: return launch_pipe_n<G, P, W, MAXR, 4>(a, stream);
-#endif
-#if SS_PIPE_MAX_RANKS >= 8
-    case 5: return launch_pipe_n<G, P, W, MAXR, 5>(a, stream);
-    case 6: return launch_pipe_n<G, P, W, MAXR, 6>(a, stream);
-    case 7: return launch_pipe_n<G, P, W, MAXR, 7>(a, stream);
-    case 8: return launch_pipe_n<G, P, W, MAXR, 8>(a, stream);
-#endif
+    SS_PIPE_CASE(1) SS_PIPE_CASE(2) SS_PIPE_CASE(3) SS_PIPE_CASE(4)
+    SS_PIPE_CASE(5) SS_PIPE_CASE(6) SS_PIPE_CASE(7) SS_PIPE_CASE(8)
     default: return SS_ERR_INVALID_ARG;
   }
+#undef SS_PIPE_CASE
 }
 
 template <int MAXR>
@@ -602,7 +600,7 @@ ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, 
   // Only reachable forms are instantiated: an fp32 gradient (gt is then the
   // placeholder SS_BF16) always travels with the small rank table and takes the
   // double-buffered, shifted or element-wise form; the double-buffered form is
-  // chosen only for at most SS_PIPE_MAX_RANKS ranks, so only with the small table.
+  // chosen only for at most 8 ranks, so only with the small table.
 #define SS_ADAM_CASE(G, P, F, W)                                                          \
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
     if (path == Path::kShift) return launch_shift<G, P, F, W, MAXR>(a, rphase, pphase, stream); \
@@ -696,7 +694,7 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
   if (n == 0) return SS_OK;
   int h = common_phase(p16, p32);
   const bool vec = h >= 0 && h < n;
-  Path path = !vec ? Path::kScalar : ((from_g32 || n_ranks <= SS_PIPE_MAX_RANKS) ? Path::kPipe : Path::kVector);
+  Path path = !vec ? Path::kScalar : ((from_g32 || pipe_ranks(n_ranks)) ? Path::kPipe : Path::kVector);
   // 16-bit arrays off the fp32 arrays' phase: per-array byte phases at the fp32 group starts
   std::vector<uint8_t> rphase(from_g32 ? 0 : n_ranks, 0);
   uint8_t pphase = 0;
