@@ -18,12 +18,13 @@ struct CopyArgs {
   int32_t esize;
 };
 
-// Body of one segment: destination-aligned 16-byte vectors. The source of
-// vector j starts SOFF bytes past a 16-byte boundary; misaligned sources are
-// read as the two aligned 16-byte chunks that hold it, and only when both
-// chunks lie inside the source range -- otherwise element by element.
+// The 16 source bytes of one destination-aligned vector at byte offset off of
+// the segment, whose start lies SOFF bytes past a 16-byte boundary: read
+// directly when SOFF == 0, else as the two aligned 16-byte chunks that hold
+// it and funnel-shifted -- only when both chunks lie inside the segment's
+// source range (direct = false otherwise: the caller copies element-wise).
 template <int SOFF>
-__device__ __forceinline__ uint4 copy_src16(const char* s, int64_t off, int64_t bytes, int esize, bool& direct) {
+__device__ __forceinline__ uint4 copy_src16(const char* s, int64_t off, int64_t bytes, bool& direct) {
   if constexpr (SOFF == 0) {
     direct = true;
     return __ldcs(reinterpret_cast<const uint4*>(s + off));
@@ -38,10 +39,7 @@ __device__ __forceinline__ uint4 copy_src16(const char* s, int64_t off, int64_t 
 }
 
 // Body of one segment: destination-aligned 16-byte vectors, kCopyUnroll per
-// thread per iteration with their loads issued first. The source of vector j
-// starts SOFF bytes past a 16-byte boundary; misaligned sources are read as
-// the two aligned 16-byte chunks that hold it, and only when both chunks lie
-// inside the source range -- otherwise element by element.
+// thread per iteration with their loads issued first (see copy_src16).
 constexpr int kCopyUnroll = 4;
 
 template <int SOFF>
@@ -54,7 +52,7 @@ __device__ __forceinline__ void copy_body(const char* s, char* d, int64_t h, int
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
       const int64_t j = j0 + u * stride;
-      v[u] = copy_src16<SOFF>(s, h + 16 * (j < nvec ? j : j0), bytes, esize, direct[u]);
+      v[u] = copy_src16<SOFF>(s, h + 16 * (j < nvec ? j : j0), bytes, direct[u]);
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
