@@ -12,15 +12,15 @@ namespace {
 // Deterministic per-shard sum of squares of the reduced gradient. The shard is
 // cut into tiles of kThreads x kSumsqGroups groups of 8 elements (after the
 // 0..7-element head that aligns the vectors); thread j of a tile owns groups
-// j, j + kThreads, ..., issues all their loads first, adds each group's 8
-// squares in fp32 (a fixed FMA chain) and the group sums in double in group
-// order as fp32 pairs (TwoSum); the block combines its threads' pairs through
-// a fixed shuffle tree and writes ONE double per tile into the caller's
-// workspace (GB300's fp64 rate is low, so fp64 is kept to one value per tile). The
-// head/tail elements (< 16) get a slot of their own. A second one-block
-// kernel adds the slots in index order. The partition depends only on n and
-// the arrays' 16-byte phase, never on the grid size, so the result is
-// bit-reproducible.
+// j, j + kThreads, ..., loads them (for up to 8 ranks pipelined across the
+// block's tiles), adds each group's 8 squares in fp32 (a fixed FMA chain) and
+// the group sums in group order as an fp32 pair (TwoSum); the block combines
+// its threads' pairs through a fixed shuffle tree and the warps in order, and
+// writes ONE double per tile into the caller's workspace (GB300's fp64 rate is
+// low, so fp64 is kept to one value per tile). The head/tail elements (< 16)
+// get a slot of their own. A second one-block kernel adds the slots in a fixed
+// order. The partition depends only on n and the arrays' 16-byte phase, never
+// on the grid size, so the result is bit-reproducible.
 //
 // Error: each 8-element fp32 chain of non-negative terms is within 8 * 2^-24
 // relative of its exact value; the fp32-pair and double sums add < 2^-40 (the
