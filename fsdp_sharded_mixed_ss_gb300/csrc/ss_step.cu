@@ -34,10 +34,10 @@ __device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float 
 }
 
 // Rank counts up to which the single-buffered kernel also prefetches its
-// warp's next groups into L2 (measured on GB300 at 2^26 elements: +7-12% for
-// N = 9-12, -4.5% at N = 16).
+// warp's next groups into L2 (measured on GB300 at 2^26 elements: +3-12% for
+// N = 5-13, none at 14, -3% at 15, -6% at 16).
 #ifndef SS_VEC_PF_RANKS
-#define SS_VEC_PF_RANKS 12
+#define SS_VEC_PF_RANKS 13
 #endif
 constexpr int kVecPrefetchRanks = SS_VEC_PF_RANKS;
 
