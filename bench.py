@@ -486,6 +486,7 @@ def run_suite(args, device) -> dict:
     del G
     del st, p16, g32, ws
     torch.cuda.empty_cache()
+    out.update(run_config_steps(ss, device, timed, entry))
     for name, numels, N, dt in (("unshard_gpt2_small_N8", [124_439_808], 8, torch.bfloat16),
                                 ("unshard_llama70b_layer_N64", [855_654_400], 64, torch.float16)):
         _, b = ss.ss_flatten_layout(numels, N)
@@ -503,6 +504,40 @@ def run_suite(args, device) -> dict:
                 timed(lambda: ss.ss_reshard(off, b, shards)), 4 * P)
             del base, off
         del shards, flat
+        torch.cuda.empty_cache()
+    return out
+
+
+def run_config_steps(ss, device, timed, entry) -> dict:
+    """The two large configurations at full size: the Llama-3-8B rank-0 shard (1,003,782,656
+    elements, 8 bf16 ranks with outliers) and the Llama-70B layer stepped as one unit (855,654,400
+    elements, 64 fp16 ranks, every shard at once, parameters written straight into the flat
+    layer buffer: the whole unit's step without a separate unshard)."""
+    import torch
+
+    import synth
+    from synth import workloads
+
+    out = {}
+    for w, whole_unit in ((workloads.llama3_8b_shard(), False), (workloads.llama70b_layer(), True)):
+        _, b = ss.ss_flatten_layout(w.numels, w.n_ranks)
+        n = int(b[-1]) if whole_unit else int(b[1])
+        dt = torch.bfloat16 if w.gdtype == synth.BF16 else torch.float16
+        G = []
+        for r in range(w.n_ranks):
+            t = torch.empty(n, dtype=dt, device=device)
+            synth.device_fill(w.grad(r, 1), t.view(torch.int16))
+            G.append(t)
+        st = [torch.empty(n, dtype=torch.float32, device=device)]
+        synth.device_fill(w.master, st[0].view(torch.int32))
+        st += [torch.zeros(n, dtype=torch.float32, device=device) for _ in range(2)]
+        p16 = torch.empty(n, dtype=dt, device=device)
+        hp = w.hp(1)
+        key = f"{w.name}_{'unit_step_into_flat' if whole_unit else 'shard_step'}"
+        out[key] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=p16), 5),
+                         (2 * w.n_ranks + 26) * n)
+        out[key]["elements"] = n
+        del G, st, p16
         torch.cuda.empty_cache()
     return out
 
