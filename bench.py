@@ -110,9 +110,24 @@ class ClockSampler:
         self.proc = None
         self.thread = None
 
+    def _smi_id(self) -> str:
+        # the device's UUID names the same physical GPU to nvidia-smi whatever CUDA_VISIBLE_DEVICES
+        # does to ordinals; the ordinal is the fallback
+        try:
+            import torch
+
+            u = getattr(torch.cuda.get_device_properties(self.index), "uuid", None)
+            u = str(u) if u else ""
+            u = u[4:] if u.startswith("GPU-") else u
+            if len(u) == 36 and all(c in "0123456789abcdefABCDEF-" for c in u):  # a real (not masked) UUID
+                return "GPU-" + u
+        except Exception:  # no torch/CUDA here: fall back to the ordinal
+            pass
+        return str(self.index)
+
     def start(self):
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", self._smi_id(), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
