@@ -18,55 +18,72 @@ struct CopyArgs {
   int32_t esize;
 };
 
-// The 16 source bytes of one destination-aligned vector at byte offset off of
-// the segment, whose start lies SOFF bytes past a 16-byte boundary: read
-// directly when SOFF == 0, else as the two aligned 16-byte chunks that hold
-// it and funnel-shifted -- only when both chunks lie inside the segment's
-// source range (direct = false otherwise: the caller copies element-wise).
-template <int SOFF>
-__device__ __forceinline__ uint4 copy_src16(const char* s, int64_t off, int64_t bytes, bool& direct) {
-  if constexpr (SOFF == 0) {
-    direct = true;
-    return __ldcs(reinterpret_cast<const uint4*>(s + off));
-  } else {
-    const char* c0 = s + off - SOFF;
-    direct = c0 >= s && (off - SOFF) + 32 <= bytes;
-    if (!direct) return make_uint4(0u, 0u, 0u, 0u);
-    const uint4 a = __ldcs(reinterpret_cast<const uint4*>(c0));
-    const uint4 b = __ldcs(reinterpret_cast<const uint4*>(c0 + 16));
-    return window16<SOFF>(a, b);
-  }
-}
+// Destination-aligned 16-byte vectors, kCopyUnroll per thread per iteration
+// with their loads issued first, when source and destination share a 16-byte
+// phase (vectors past the end re-read vector j0, in range, and are not stored).
+constexpr int kCopyUnroll = 8;
 
-// Body of one segment: destination-aligned 16-byte vectors, kCopyUnroll per
-// thread per iteration with their loads issued first (see copy_src16).
-constexpr int kCopyUnroll = 4;
-
-template <int SOFF>
-__device__ __forceinline__ void copy_body(const char* s, char* d, int64_t h, int64_t nvec, int64_t bytes, int esize,
-                                          int64_t tid, int64_t stride) {
+__device__ __forceinline__ void copy_body_aligned(const char* s, char* d, int64_t h, int64_t nvec, int64_t tid,
+                                                  int64_t stride) {
   for (int64_t j0 = tid; j0 < nvec; j0 += stride * kCopyUnroll) {
-    // all loads first; a vector past the end re-reads vector j0 (in range) and is not stored
     uint4 v[kCopyUnroll];
-    bool direct[kCopyUnroll];
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
       const int64_t j = j0 + u * stride;
-      v[u] = copy_src16<SOFF>(s, h + 16 * (j < nvec ? j : j0), bytes, direct[u]);
+      v[u] = __ldcs(reinterpret_cast<const uint4*>(s + h + 16 * (j < nvec ? j : j0)));
     }
 #pragma unroll
     for (int u = 0; u < kCopyUnroll; ++u) {
       const int64_t j = j0 + u * stride;
-      if (j >= nvec) break;
-      const int64_t off = h + 16 * j;
-      if (direct[u]) {
-        __stcs(reinterpret_cast<uint4*>(d + off), v[u]);
-      } else {
-        for (int i = 0; i < 16; i += esize) {
-          if (esize == 2) *reinterpret_cast<uint16_t*>(d + off + i) = *reinterpret_cast<const uint16_t*>(s + off + i);
-          else *reinterpret_cast<uint32_t*>(d + off + i) = *reinterpret_cast<const uint32_t*>(s + off + i);
-        }
+      if (j < nvec) __stcs(reinterpret_cast<uint4*>(d + h + 16 * j), v[u]);
+    }
+  }
+}
+
+// Destination-aligned vectors whose source lies SOFF (2..14) bytes past a
+// 16-byte boundary, warp-cooperatively: vector j's 16 bytes are the window at
+// SOFF into source chunks j and j + 1 (aligned, chunk j at s + h - SOFF + 16 j).
+// A warp takes blocks of 32 x kCopyUnroll consecutive vectors; lane l loads
+// chunk (block start + 32 u + l) for each u and takes chunk + 1 from lane l + 1
+// by shuffle (lane 31 from lane 0's next chunk, or, after the last u, from one
+// extra load), so each source byte is loaded once. Body: vectors 1 .. nvec-2,
+// whose chunks 1 .. nvec-1 all lie inside the segment's source range; vectors
+// 0 and nvec - 1 are copied element by element with the head and tail.
+template <int SOFF>
+__device__ __forceinline__ void copy_body_shifted(const char* s, char* d, int64_t h, int64_t nvec, int64_t warp,
+                                                  int64_t nwarps, int lane) {
+  constexpr int U = kCopyUnroll;
+  const char* c0 = s + h - SOFF;
+  const int64_t last = nvec - 1;  // the highest chunk index read
+  for (int64_t v0 = 1 + warp * 32 * U; v0 < last; v0 += nwarps * 32 * U) {  // warp-uniform
+    uint4 c[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      int64_t j = v0 + u * 32 + lane;
+      j = j < last ? j : last;
+      c[u] = __ldcs(reinterpret_cast<const uint4*>(c0 + 16 * j));
+    }
+    uint4 extra = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 31) {
+      int64_t j = v0 + U * 32;
+      j = j < last ? j : last;
+      extra = __ldcs(reinterpret_cast<const uint4*>(c0 + 16 * j));
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      uint4 nb = make_uint4(__shfl_down_sync(0xFFFFFFFFu, c[u].x, 1), __shfl_down_sync(0xFFFFFFFFu, c[u].y, 1),
+                            __shfl_down_sync(0xFFFFFFFFu, c[u].z, 1), __shfl_down_sync(0xFFFFFFFFu, c[u].w, 1));
+      if (u + 1 < U) {
+        const uint4 f = make_uint4(__shfl_sync(0xFFFFFFFFu, c[u + 1 < U ? u + 1 : u].x, 0),
+                                   __shfl_sync(0xFFFFFFFFu, c[u + 1 < U ? u + 1 : u].y, 0),
+                                   __shfl_sync(0xFFFFFFFFu, c[u + 1 < U ? u + 1 : u].z, 0),
+                                   __shfl_sync(0xFFFFFFFFu, c[u + 1 < U ? u + 1 : u].w, 0));
+        if (lane == 31) nb = f;
+      } else if (lane == 31) {
+        nb = extra;
       }
+      const int64_t v = v0 + u * 32 + lane;
+      if (v < last) __stcs(reinterpret_cast<uint4*>(d + h + 16 * v), window16<SOFF>(c[u], nb));
     }
   }
 }
@@ -87,20 +104,37 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
   const int soff = static_cast<int>(reinterpret_cast<uintptr_t>(s + h) & 15u);
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t warp = tid >> 5, nwarps = stride >> 5;
+  const int lane = threadIdx.x & 31;
   switch (soff) {
-    case 0: copy_body<0>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 2: copy_body<2>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 4: copy_body<4>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 6: copy_body<6>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 8: copy_body<8>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 10: copy_body<10>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    case 12: copy_body<12>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
-    default: copy_body<14>(s, d, h, nvec, bytes, a.esize, tid, stride); break;
+    case 0: copy_body_aligned(s, d, h, nvec, tid, stride); break;
+    case 2: copy_body_shifted<2>(s, d, h, nvec, warp, nwarps, lane); break;
+    case 4: copy_body_shifted<4>(s, d, h, nvec, warp, nwarps, lane); break;
+    case 6: copy_body_shifted<6>(s, d, h, nvec, warp, nwarps, lane); break;
+    case 8: copy_body_shifted<8>(s, d, h, nvec, warp, nwarps, lane); break;
+    case 10: copy_body_shifted<10>(s, d, h, nvec, warp, nwarps, lane); break;
+    case 12: copy_body_shifted<12>(s, d, h, nvec, warp, nwarps, lane); break;
+    default: copy_body_shifted<14>(s, d, h, nvec, warp, nwarps, lane); break;
   }
-  // head (h bytes) and tail (bytes - t0) element by element
+  // Element by element: the head (h bytes) and the tail (bytes - t0), and with
+  // a shifted source also vectors 0 and nvec - 1 (or every vector when nvec <
+  // 3): at most 62 bytes, one element per thread of the segment's first block.
+  const int64_t ve = soff == 0 ? 0 : (nvec < 3 ? nvec : 2);  // edge vectors copied here
+  const int64_t eb = 16 / a.esize;                            // elements per vector
   const int64_t nh = h / a.esize, nt = (bytes - t0) / a.esize;
-  if (tid < nh + nt) {
-    const int64_t off = tid < nh ? tid * a.esize : t0 + (tid - nh) * a.esize;
+  if (blockIdx.x == 0 && threadIdx.x < nh + nt + ve * eb) {
+    const int64_t i = threadIdx.x;
+    int64_t off;
+    if (i < nh) {
+      off = i * a.esize;
+    } else if (i < nh + nt) {
+      off = t0 + (i - nh) * a.esize;
+    } else {
+      const int64_t q = i - nh - nt;                  // element q of the edge vectors
+      const int64_t vec = q / eb;                     // 0, 1 (or up to 2 when nvec < 3)
+      const int64_t vi = (nvec < 3) ? vec : (vec == 0 ? 0 : nvec - 1);
+      off = h + 16 * vi + (q % eb) * a.esize;
+    }
     if (a.esize == 2) *reinterpret_cast<uint16_t*>(d + off) = *reinterpret_cast<const uint16_t*>(s + off);
     else *reinterpret_cast<uint32_t*>(d + off) = *reinterpret_cast<const uint32_t*>(s + off);
   }
