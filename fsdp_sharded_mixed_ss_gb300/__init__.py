@@ -93,8 +93,6 @@ def _load():
     lib.ss_grad_sumsq.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, i64, vp, vp, vp]
     lib.ss_clip_coef.argtypes = [vp, i32, f32, vp, vp, vp]
     lib.ss_grad_sumsq_noalloc.argtypes = [i64, vp, vp, i32, i32, f32, vp, vp, vp, vp]
-    lib.ss_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), i32]
-    lib.ss_selftest_wait_timeout.argtypes = [i64, vp]
     return lib
 
 
@@ -187,19 +185,6 @@ def _addr(a: array.array | None) -> int | None:
 
 def ss_abi_version() -> int:
     return int(_lib.ss_abi_version())
-
-
-def ss_device_error(clear: bool = False) -> int:
-    """The library's device error word on the current device (waits for queued work)."""
-    w = ctypes.c_uint32(0)
-    _check(_lib.ss_device_error(ctypes.byref(w), int(bool(clear))), "ss_device_error")
-    return int(w.value)
-
-
-def ss_selftest_wait_timeout(limit_ns: int, *, stream=None) -> None:
-    """Launch one block whose bounded wait runs out after limit_ns and sets bit 0 of the device
-    error word (a failure-reporting test without a fault)."""
-    _check(_lib.ss_selftest_wait_timeout(int(limit_ns), _stream(stream)), "ss_selftest_wait_timeout")
 
 
 def ss_flatten_layout(numels: Sequence[int], n_ranks: int):

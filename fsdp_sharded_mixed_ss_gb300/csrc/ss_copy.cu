@@ -1,7 +1,7 @@
 // ss_copy.cu -- unshard / reshard: the gather copy of the ranks' shards into the
-// flat unit buffer and its inverse, on the bulk-copy (TMA) engine when every
-// segment keeps its 16-byte phase, else on SIMT threads; and the library's
-// device error word raised by the bulk copy's bounded waits.
+// flat unit buffer and its inverse, one launch over all shards: 16-byte
+// vectors aligned on the destination, the source read directly when it shares
+// the destination's 16-byte phase and warp-cooperatively shifted otherwise.
 #include "ss_common.cuh"
 
 namespace ss {
@@ -21,7 +21,10 @@ struct CopyArgs {
 // Destination-aligned 16-byte vectors, kCopyUnroll per thread per iteration
 // with their loads issued first, when source and destination share a 16-byte
 // phase (vectors past the end re-read vector j0, in range, and are not stored).
-constexpr int kCopyUnroll = 8;
+// Sixteen vectors (256 bytes) in flight per thread measured fastest on GB300:
+// 2-5% above a cp.async.bulk (TMA) global -> shared -> global copy with four
+// 16 KB chunks in flight per block, on every size and shard count tried.
+constexpr int kCopyUnroll = 16;
 
 __device__ __forceinline__ void copy_body_aligned(const char* s, char* d, int64_t h, int64_t nvec, int64_t tid,
                                                   int64_t stride) {
@@ -140,222 +143,23 @@ __global__ void __launch_bounds__(kThreads) copy_segments_kernel(const __grid_co
   }
 }
 
-// ------------------------------------------------------------------ unshard / reshard with the bulk-copy engine
-//
-// When every segment's source and destination share a 16-byte phase, the copy
-// is handed to the TMA engine: a one-warp block streams its chunks of a
-// segment global -> shared -> global with cp.async.bulk, kTmaSlots chunks of
-// kTmaChunk bytes in flight (loads completed on an mbarrier, stores tracked as
-// bulk groups). The threads only issue copies, so a few blocks per SM keep
-// ~200 KB moving. The 0..14 bytes before the first 16-byte boundary and the
-// 0..14 after the last are copied element by element.
-//
-// Each mbarrier wait is bounded (about one second of %globaltimer); on expiry
-// the block records bit 0 in the library's device error word
-// (ss_device_error), lets its copies in flight land (bounded again) and
-// returns instead of hanging.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-#ifndef SS_TMA_CHUNK
-#define SS_TMA_CHUNK 16384
-#endif
-#ifndef SS_TMA_SLOTS
-#define SS_TMA_SLOTS 4
-#endif
-constexpr int kTmaChunk = SS_TMA_CHUNK;
-constexpr int kTmaSlots = SS_TMA_SLOTS;
-enum : uint32_t { SS_DEVERR_TIMEOUT = 1u };
-
-__device__ uint32_t g_device_error = 0;
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0u;
-}
-
-// Wait for the phase of the given parity to complete, for at most limit_ns
-// (~1 s by default); on expiry set the timeout bit of the device error word
-// and return false.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (;;) {
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > limit_ns) {
-      atomicOr(&g_device_error, SS_DEVERR_TIMEOUT);
-      return false;
-    }
-  }
-}
-
-// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
-// arrives at, so the wait runs out after limit_ns and reports through the
-// device error word, exactly as a bulk-copy wait would. Nothing is in flight
-// on the barrier, so the block simply returns.
-__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint64_t limit_ns) {
-  pdl_wait();
-  pdl_trigger();
-  __shared__ __align__(8) uint64_t bar;
-  if (threadIdx.x != 0) return;
-  const uint32_t b = smem_addr(&bar);
-  mbar_init(b, 1u);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  mbar_wait(b, 0u, limit_ns);
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-// Global -> shared; bytes and both addresses multiples of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
-
-// Shared -> global; bytes and both addresses multiples of 16.
-__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-template <int MAXR>
-__global__ void __launch_bounds__(32) copy_tma_kernel(const __grid_constant__ CopyArgs<MAXR> a) {
-  pdl_wait();
-  pdl_trigger();
-  extern __shared__ __align__(128) unsigned char buf[];  // [kTmaSlots][kTmaChunk]
-  __shared__ __align__(8) uint64_t bars[kTmaSlots];
-  const int k = blockIdx.y;
-  const int64_t bytes = a.bytes[k];
-  if (bytes == 0) return;
-  const char* s = static_cast<const char*>(a.src[k]);
-  char* d = static_cast<char*>(a.dst[k]);
-  int64_t h = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(d) & 15u)) & 15u);
-  if (h > bytes) h = bytes;
-  const int64_t body = ((bytes - h) / 16) * 16;
-  const int lane = threadIdx.x;
-  // head and tail (< 16 bytes each), element by element, in block 0 of the segment
-  if (blockIdx.x == 0) {
-    const int64_t nh = h / a.esize, nt = (bytes - h - body) / a.esize;
-    if (lane < nh + nt) {
-      const int64_t off = lane < nh ? lane * a.esize : h + body + (lane - nh) * a.esize;
-      if (a.esize == 2) *reinterpret_cast<uint16_t*>(d + off) = *reinterpret_cast<const uint16_t*>(s + off);
-      else *reinterpret_cast<uint32_t*>(d + off) = *reinterpret_cast<const uint32_t*>(s + off);
-    }
-  }
-  if (lane != 0) return;
-  const uint32_t bar0 = smem_addr(bars), buf0 = smem_addr(buf);
-  for (int i = 0; i < kTmaSlots; ++i) mbar_init(bar0 + 8u * i, 1u);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  const int64_t nch = (body + kTmaChunk - 1) / kTmaChunk;
-  const int64_t bx = blockIdx.x, gx = gridDim.x;
-  const int64_t cnt = nch > bx ? (nch - bx + gx - 1) / gx : 0;  // chunks bx, bx + gx, ...
-  auto chunk_bytes = [&](int64_t i) {
-    const int64_t left = body - (bx + i * gx) * kTmaChunk;
-    return static_cast<uint32_t>(left < kTmaChunk ? left : kTmaChunk);
-  };
-  auto issue = [&](int64_t i) {
-    const uint32_t slot = static_cast<uint32_t>(i % kTmaSlots);
-    const uint32_t nb = chunk_bytes(i);
-    mbar_expect_tx(bar0 + 8u * slot, nb);
-    bulk_load(buf0 + slot * kTmaChunk, s + h + (bx + i * gx) * kTmaChunk, nb, bar0 + 8u * slot);
-  };
-  const int64_t first = cnt < kTmaSlots ? cnt : kTmaSlots;
-  for (int64_t i = 0; i < first; ++i) issue(i);
-  int64_t issued = first, i = 0;
-  for (; i < cnt; ++i) {
-    const uint32_t slot = static_cast<uint32_t>(i % kTmaSlots);
-    if (!mbar_wait(bar0 + 8u * slot, static_cast<uint32_t>((i / kTmaSlots) & 1))) break;
-    bulk_store(d + h + (bx + i * gx) * kTmaChunk, buf0 + slot * kTmaChunk, chunk_bytes(i));
-    bulk_commit();
-    if (issued < cnt) {
-      bulk_wait_read_all();  // the store just issued has read its slot: the slot may be refilled
-      issue(issued++);
-    }
-  }
-  bulk_wait_all();
-  // after a timed-out wait: let the loads already issued land before the block exits
-  for (int64_t j = i + 1; j < issued; ++j)
-    mbar_wait(bar0 + 8u * static_cast<uint32_t>(j % kTmaSlots), static_cast<uint32_t>((j / kTmaSlots) & 1));
-}
-
-// Raise a kernel's dynamic shared memory limit once per device (cached per device and kernel).
-bool allow_smem(const void* fn, size_t bytes) {
-  struct Done {
-    int dev;
-    const void* fn;
-    size_t bytes;
-  };
-  static std::mutex mu;
-  static std::vector<Done> done;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return false;
-  std::lock_guard<std::mutex> lock(mu);
-  for (const Done& d : done)
-    if (d.dev == dev && d.fn == fn && d.bytes >= bytes) return true;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) != cudaSuccess)
-    return false;
-  done.push_back({dev, fn, bytes});
-  return true;
-}
-
 template <int MAXR>
 ss_status run_copy(const void* const* src, void* const* dst, const int64_t* bytes, int32_t n_seg, int32_t esize,
                    int64_t total_bytes, void* stream) {
   CopyArgs<MAXR> a;
   std::memset(&a, 0, sizeof a);
-  bool same_phase = true;
   for (int32_t k = 0; k < n_seg; ++k) {
     a.src[k] = src[k];
     a.dst[k] = dst[k];
     a.bytes[k] = bytes[k];
-    if (bytes[k] > 0 && ((reinterpret_cast<uintptr_t>(src[k]) - reinterpret_cast<uintptr_t>(dst[k])) & 15u) != 0)
-      same_phase = false;
   }
   a.n_seg = n_seg;
   a.esize = esize;
-  if (same_phase && total_bytes >= (int64_t{1} << 20)) {
-    // bulk-copy engine: one-warp blocks, kTmaSlots chunks in flight each
-    auto* fn = copy_tma_kernel<MAXR>;
-    const size_t smem = static_cast<size_t>(kTmaSlots) * kTmaChunk;
-    const void* f = reinterpret_cast<const void*>(fn);
-    if (!allow_smem(f, smem)) return cuda_fail(cudaGetLastError());
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, 32, smem) != cudaSuccess || per_sm < 1) per_sm = 1;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
-    const int64_t chunks = (total_bytes / std::max(1, n_seg)) / kTmaChunk + 1;
-    const int64_t gx = std::max<int64_t>(1, std::min<int64_t>((cap + n_seg - 1) / n_seg, chunks));
-    return launch_dependent(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg)), dim3(32), smem, stream, a);
-  }
   auto* fn = copy_segments_kernel<MAXR>;
   const int64_t cap = std::max<int64_t>(1, static_cast<int64_t>(sm_count()) * blocks_per_sm(reinterpret_cast<const void*>(fn)));
   const int64_t per_seg_work = (total_bytes / std::max(1, n_seg)) / 16 + 1;
-  int64_t gx = std::min<int64_t>((cap + n_seg - 1) / n_seg, (per_seg_work + kThreads - 1) / kThreads);
+  // one wave: at most cap / n_seg blocks per segment (a partial second wave would double the tail)
+  int64_t gx = std::min<int64_t>(cap / n_seg, (per_seg_work + kThreads - 1) / kThreads);
   gx = std::max<int64_t>(gx, 1);
   return launch_dependent(fn, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(n_seg)), dim3(kThreads), 0, stream, a);
 }
@@ -366,24 +170,6 @@ ss_status run_copy(const void* const* src, void* const* dst, const int64_t* byte
 using namespace ss;
 
 extern "C" {
-
-ss_status ss_selftest_wait_timeout(int64_t limit_ns, void* stream) {
-  if (limit_ns < 1000000 || limit_ns > 2000000000) return SS_ERR_INVALID_ARG;
-  return launch_dependent(wait_timeout_selftest_kernel, dim3(1), dim3(32), 0, stream,
-                          static_cast<uint64_t>(limit_ns));
-}
-
-ss_status ss_device_error(uint32_t* out, int32_t clear) {
-  if (!out) return SS_ERR_INVALID_ARG;
-  cudaError_t e = cudaMemcpyFromSymbol(out, g_device_error, sizeof(uint32_t));
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (clear) {
-    const uint32_t zero = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(uint32_t));
-    if (e != cudaSuccess) return cuda_fail(e);
-  }
-  return SS_OK;
-}
 
 static ss_status copy_common(const void* const* src, void* const* dst, const int64_t* shard_bounds, int32_t n_ranks,
                              ss_dtype dtype, bool unshard, void* stream) {

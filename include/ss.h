@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define SS_ABI_VERSION 1
+#define SS_ABI_VERSION 2
 #define SS_MAX_RANKS 1024
 
 typedef enum ss_status {
@@ -241,9 +241,9 @@ ss_status ss_grad_sumsq_noalloc(int64_t n, const float* g32, const void* const* 
  *   shard_bounds[0] = 0). dtype: SS_BF16, SS_FP16 or SS_FP32. One launch.
  * ss_reshard: the reverse copy, flat -> shards.
  * Bit-exact copies. Shards must not overlap the flat buffer or each other.
- * When every shard and its place in the flat buffer share a 16-byte phase
- * (and the unit is at least 1 MiB) the copy runs on the bulk-copy (TMA)
- * engine; otherwise on vector loads and stores. */
+ * 16-byte vector stores aligned on the destination; a shard whose place in
+ * the flat buffer is not at its own 16-byte phase is read as aligned 16-byte
+ * chunks and shifted in registers (same results, about the same bandwidth). */
 ss_status ss_unshard(const void* const* shards, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
                      void* flat, void* stream);
 ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ranks, ss_dtype dtype,
@@ -253,21 +253,6 @@ ss_status ss_reshard(const void* flat, const int64_t* shard_bounds, int32_t n_ra
 const char* ss_status_string(ss_status s);      /* static string, never NULL */
 const char* ss_last_cuda_error(void);           /* last CUDA error text of this thread ("" if none) */
 
-/* The library's device error word on the current device. Bit 0 (value 1): a
- * bulk-copy wait in an unshard/reshard kernel gave up after about one second
- * and the kernel returned early, so that copy is incomplete. Copies the word
- * to *out (host) and, when clear != 0, resets it. Synchronous: it waits for
- * the work already queued on the device. */
-ss_status ss_device_error(uint32_t* out, int32_t clear);
-
-/* Self-test of the bounded-wait path (no counterpart on the pages): launches,
- * on `stream`, one block that waits on a shared-memory barrier nothing ever
- * completes, using the same bounded wait as the bulk-copy kernel but with a
- * limit of limit_ns nanoseconds (1e6 .. 2e9, else SS_ERR_INVALID_ARG and
- * nothing is launched). The wait runs out, sets bit 0 of the device error
- * word and the block returns; the context stays usable. For testing failure
- * reporting without a fault: clear the word afterwards. */
-ss_status ss_selftest_wait_timeout(int64_t limit_ns, void* stream);
 int32_t ss_abi_version(void);                   /* SS_ABI_VERSION */
 
 #ifdef __cplusplus

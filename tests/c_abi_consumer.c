@@ -77,7 +77,6 @@ static void host_checks(void) {
   CHECK(ss_grad_reduce(ranks, 2, SS_FP32, 64, 1.0f, 0, fake + 128, NULL, NULL) == SS_ERR_DTYPE);
   CHECK(ss_grad_reduce(ranks, 2, SS_BF16, -1, 1.0f, 0, fake + 128, NULL, NULL) == SS_ERR_INVALID_ARG);
   CHECK(ss_grad_sumsq_workspace(-1) == -1 && ss_grad_sumsq_workspace(16384) == 8 * 3);
-  CHECK(ss_selftest_wait_timeout(0, NULL) == SS_ERR_INVALID_ARG);
 }
 
 #ifdef SS_WITH_CUDA
@@ -158,8 +157,6 @@ static void gpu_checks(void) {
     for (int64_t j = 0; j < len; ++j) bad += h32[j] != (float)(bnd[k] + j);
   }
   CHECK(bad == 0);
-  uint32_t word = 1;
-  CHECK(ss_device_error(&word, 0) == SS_OK && word == 0);
   CHECK(cudaDeviceSynchronize() == cudaSuccess);
 
   for (int k = 0; k < 7; ++k) cudaFree(shards[k]);

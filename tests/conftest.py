@@ -48,15 +48,3 @@ def built_libraries():
         mod.build()
     yield
 
-
-@pytest.fixture(autouse=True)
-def no_device_errors(request):
-    """After every GPU test: no kernel of the library gave up on a bounded wait."""
-    yield
-    if "gpu" not in request.keywords:
-        return
-    import torch
-    if not torch.cuda.is_available():
-        return
-    import fsdp_sharded_mixed_ss_gb300 as ss
-    assert ss.ss_device_error(clear=True) == 0, "a bulk-copy wait timed out"

@@ -36,7 +36,7 @@ def test_every_declared_symbol_is_exported(ss):
     lib = ctypes.CDLL(ss.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), n
-    assert ss.ss_abi_version() == 1
+    assert ss.ss_abi_version() == 2
 
 
 @pytest.mark.parametrize("numels,N", [(workloads.tiny_mlp_numels(), 4), (workloads.gpt2_small_numels(), 8),
@@ -154,14 +154,6 @@ def test_sumsq_and_clip_argument_errors(ss):
     with pytest.raises(ss.SSError) as e:
         ss.ss_clip_coef(O, 4, 1.0, O + 8, stream=0)  # coefficient overlaps the shard sums
     assert e.value.status == 3
-
-
-def test_wait_selftest_limit_checked_on_host(ss):
-    # the bounded-wait self-test only accepts limits of 1 ms .. 2 s, and says so before any launch
-    for bad in (0, 999_999, 2_000_000_001, -5):
-        with pytest.raises(ss.SSError) as e:
-            ss.ss_selftest_wait_timeout(bad, stream=0)
-        assert e.value.status == 1
 
 
 def test_noalloc_size_limit_rejected_on_host(ss):
