@@ -295,6 +295,30 @@ def test_unshard_into_offset_flat(ss):
         assert (base[:off] == 0).all() and (base[off + P:] == 0).all()
 
 
+@pytest.mark.parametrize("N,off,dtname", [(8, 1, "bfloat16"), (64, 3, "bfloat16"), (7, 1, "float32"),
+                                           (1, 5, "float16")])
+def test_unshard_reshard_large_off_phase(ss, N, off, dtname):
+    """2^26 + 13 elements with the flat buffer `off` elements past a 16-byte boundary: every
+    segment takes the warp-cooperative shifted reads over many warp iterations; the round trip is
+    bit-exact and nothing outside the flat view is written."""
+    import torch
+    dt = getattr(torch, dtname)
+    P = (1 << 26) + 13
+    _, b = ss.ss_flatten_layout([P], N)
+    src = torch.arange(P, device="cuda", dtype=torch.int32)
+    iv = torch.int32 if dt == torch.float32 else torch.int16
+    shards = [src[int(b[k]):int(b[k + 1])].to(iv).view(dt).clone() for k in range(N)]
+    base = torch.zeros(P + 16, dtype=dt, device="cuda")
+    flat = base[off:off + P]
+    ss.ss_unshard(shards, b, flat)
+    assert torch.equal(flat.view(iv), torch.cat([t.view(iv) for t in shards]))
+    assert (base.view(iv)[:off] == 0).all() and (base.view(iv)[off + P:] == 0).all()
+    back = [torch.zeros(int(b[k + 1] - b[k]), dtype=dt, device="cuda") for k in range(N)]
+    ss.ss_reshard(flat, b, back)
+    for x, y in zip(back, shards):
+        assert torch.equal(x.view(iv), y.view(iv))
+
+
 def test_step_split_calls_agree(ss):
     """A shard stepped in two calls (a short one and a long one) gets the same bits as in one call."""
     import torch
