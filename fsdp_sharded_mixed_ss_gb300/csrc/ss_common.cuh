@@ -258,9 +258,11 @@ inline bool is16(ss_dtype d) { return d == SS_BF16 || d == SS_FP16; }
 
 // Launches fn<<<grid, block, smem, stream>>>(args...) as a programmatic
 // dependent of the previous kernel in the stream (see pdl_wait). Every kernel
-// of the library starts with pdl_wait() and pdl_trigger(), and every grid is
-// at most one wave, so all of a grid's blocks are resident before any of them
-// lets the next kernel launch.
+// of the library starts with pdl_wait() and pdl_trigger(). The next kernel can
+// launch only once every block of this grid has triggered, i.e. has started,
+// so its waiting blocks never hold resources this grid's blocks still need;
+// grids are sized to one wave (all but a copy of more shards than resident
+// blocks), which lets the next launch overlap this grid's last blocks.
 template <typename... Params, typename... Args>
 ss_status launch_dependent(void (*fn)(Params...), dim3 grid, dim3 block, size_t smem, void* stream, Args... args) {
   cudaLaunchConfig_t cfg = {};
