@@ -158,28 +158,61 @@ __device__ __forceinline__ void pipe_load(const StepArgs<MAXR>& a, int64_t gi, P
   G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + e) + 1);
 }
 
+// Work division: a chunk is 32 consecutive groups, one per lane of a warp.
+// Sweep s of the grid covers chunks [s * gridDim.x * W, (s + 1) * gridDim.x * W)
+// with W = warps per block, and block b owns the W chunks at b * W of every
+// sweep (the grid moves through the arrays front to back, as a grid-stride loop
+// would). A block's warps take its chunks in order from a counter in shared
+// memory, so a warp whose loads come back sooner takes more of them and the
+// block's warps finish together. Measured on GB300 (GPT-2 shard, N = 8): with
+// one fixed chunk per warp and sweep, warp finishing times within an SM spread
+// over ~9 us of a ~100 us kernel, with the shared counter over ~3 us; one block
+// of 512 threads per SM (128 registers a thread) lets all 16 warps of an SM
+// share one counter.
+#ifndef SS_PIPE_THREADS
+#define SS_PIPE_THREADS 512
+#endif
+constexpr int kPipeThreads = SS_PIPE_THREADS;
+constexpr int kPipeWarps = kPipeThreads / 32;
+constexpr int kPipeBlocksPerSm = 512 / kPipeThreads;  // at 128 registers a thread
+
 template <int GT, int PT, bool F, bool WRITE_P16, int MAXR, int NR>
-__global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+__global__ void __launch_bounds__(kPipeThreads, kPipeBlocksPerSm) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  __shared__ unsigned next_chunk;
+  if (threadIdx.x == 0) next_chunk = 0;
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
+  const int64_t nchunk = (nvec + 31) / 32;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t per_sweep = static_cast<int64_t>(gridDim.x) * kPipeWarps;
+  const int lane = threadIdx.x & 31;
+  // the warp's next chunk (>= nchunk once the block's chunks are all taken)
+  auto take = [&]() -> int64_t {
+    unsigned j = 0;
+    if (lane == 0) j = atomicAdd(&next_chunk, 1u);
+    j = __shfl_sync(0xFFFFFFFFu, j, 0);
+    return static_cast<int64_t>(j / kPipeWarps) * per_sweep + static_cast<int64_t>(blockIdx.x) * kPipeWarps +
+           (j % kPipeWarps);
+  };
   bool bad = false;
   PipeGroup<NR> cur, nxt;
-  if (tid < nvec) pipe_load<GT, NR, F>(a, tid, cur);
-  const int lane = threadIdx.x & 31;
-  for (int64_t gi = tid; gi < nvec; gi += stride) {
-    if (gi + stride < nvec) pipe_load<GT, NR, F>(a, gi + stride, nxt);
+  int64_t c = take();
+  int64_t cn = c < nchunk ? take() : nchunk;
+  if (c < nchunk && c * 32 + lane < nvec) pipe_load<GT, NR, F>(a, c * 32 + lane, cur);
+  while (c < nchunk) {
+    const int64_t cnn = cn < nchunk ? take() : nchunk;
+    if (cn < nchunk && cn * 32 + lane < nvec) pipe_load<GT, NR, F>(a, cn * 32 + lane, nxt);
     if constexpr (F || NR <= kPipePrefetchRanks) {
-      // L2 prefetch of the warp's groups two iterations ahead, one bulk prefetch per array
-      // (lane k takes array k): more bytes in flight without registers, for groups whose own
-      // loads are few. Hints only; every range lies inside its array.
+      // L2 prefetch of the warp's chunk after next, one bulk prefetch per array (lane k takes
+      // array k): more bytes in flight without registers, for groups whose own loads are few.
+      // Hints only; every range lies inside its array.
       constexpr int kArrays = (F ? 1 : NR) + 3;
-      const int64_t b = (gi - lane) + 2 * stride;
-      if (b < nvec && lane < kArrays) {
+      const int64_t b = cnn * 32;
+      if (cnn < nchunk && lane < kArrays) {
         const int64_t cnt = nvec - b < 32 ? nvec - b : 32;
         const int64_t e = a.head + b * kGroup;
         const char* base;
@@ -198,40 +231,45 @@ __global__ void __launch_bounds__(kThreads, 2) adam_pipe_kernel(const __grid_con
         prefetch_l2(base, static_cast<uint32_t>(bytes));
       }
     }
-    const int64_t e = a.head + gi * kGroup;
-    float g[8];
-    if constexpr (F) {
-      const uint4 x = cur.r[0], y = cur.r[1];
-      g[0] = __uint_as_float(x.x); g[1] = __uint_as_float(x.y); g[2] = __uint_as_float(x.z); g[3] = __uint_as_float(x.w);
-      g[4] = __uint_as_float(y.x); g[5] = __uint_as_float(y.y); g[6] = __uint_as_float(y.z); g[7] = __uint_as_float(y.w);
-    } else {
-      widen8<GT>(cur.r[0], g);
+    const int64_t gi = c * 32 + lane;
+    if (gi < nvec) {
+      const int64_t e = a.head + gi * kGroup;
+      float g[8];
+      if constexpr (F) {
+        const uint4 x = cur.r[0], y = cur.r[1];
+        g[0] = __uint_as_float(x.x); g[1] = __uint_as_float(x.y); g[2] = __uint_as_float(x.z); g[3] = __uint_as_float(x.w);
+        g[4] = __uint_as_float(y.x); g[5] = __uint_as_float(y.y); g[6] = __uint_as_float(y.z); g[7] = __uint_as_float(y.w);
+      } else {
+        widen8<GT>(cur.r[0], g);
 #pragma unroll
-      for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
-      if (a.post_scale != 1.0f) {
+        for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
+        if (a.post_scale != 1.0f) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+          for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+        }
       }
-    }
-    if (a.nonfinite) {
+      if (a.nonfinite) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-    }
-    if (a.g_out) st8f(a.g_out + e, g);
-    if (a.dev_scale) {
+        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+      }
+      if (a.g_out) st8f(a.g_out + e, g);
+      if (a.dev_scale) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
-    }
-    float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
-    float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
-    float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+      }
+      float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
+      float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
+      float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
-    st8f(a.master + e, p);
-    st8f(a.m + e, m);
-    st8f(a.v + e, v);
-    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+      for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+      st8f(a.master + e, p);
+      st8f(a.m + e, m);
+      st8f(a.v + e, v);
+      if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+    }
     cur = nxt;
+    c = cn;
+    cn = cnn;
   }
   // the (< 8) elements before the aligned body and the (< 8) after it
   const int64_t tail0 = a.head + nvec * kGroup;
@@ -577,7 +615,8 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
 template <int G, int P, bool W, int MAXR, int NR, bool F = false>
 ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
   auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
-  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream);
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kPipeThreads), a, stream,
+                kPipeThreads);
 }
 
 template <int G, int P, bool W, int MAXR>
