@@ -45,15 +45,15 @@
 namespace ss {
 
 constexpr int kThreads = 256;
-// Block shape of the fused step kernel (the register-heavy one): threads per
-// block and the minimum resident blocks per SM asked of the compiler.
-#ifndef SS_STEP_THREADS
-#define SS_STEP_THREADS 256
+// Block shape of the fused step kernels whose warps take chunks of work from a
+// counter in shared memory (the register-heavy ones): 512 threads, one block
+// per SM at 128 registers a thread, so all 16 warps of an SM share one counter.
+#ifndef SS_CHUNK_THREADS
+#define SS_CHUNK_THREADS 512
 #endif
-#ifndef SS_STEP_MIN_BLOCKS
-#define SS_STEP_MIN_BLOCKS 1
-#endif
-constexpr int kStepThreads = SS_STEP_THREADS;
+constexpr int kChunkThreads = SS_CHUNK_THREADS;
+constexpr int kChunkWarps = kChunkThreads / 32;
+constexpr int kChunkBlocksPerSm = 512 / kChunkThreads;
 constexpr int kGroup = 8;         // elements per thread per iteration
 constexpr int kSmallRanks = 64;   // pointer table size of the common kernels
 constexpr int kLargeRanks = SS_MAX_RANKS;

@@ -11,6 +11,50 @@
 namespace ss {
 namespace {
 
+// ------------------------------------------------------------------ work division
+//
+// The vector and double-buffered step kernels run one wave of blocks, one per
+// SM. A chunk is 32 consecutive 8-element groups, one per lane of a warp; each
+// block owns a fixed set of chunks and its warps take them in order from a
+// counter in shared memory, so a warp whose loads come back sooner takes more
+// of them and the 16 warps of an SM finish together. Measured on GB300 (GPT-2
+// shard, N = 8, per-warp timer stamps in a probe build): with one fixed chunk
+// per warp and pass over the grid the warps of an SM finished up to ~9 us
+// apart in a ~100 us launch, with the counter within ~3 us.
+//
+// Which chunks block b of B owns: round robin, chunks b, b + B, b + 2B, ...
+// (the blocks' counts differ by at most one); or ADJACENT: W adjacent chunks
+// (W = warps per block) of every full pass of the grid over W * B chunks, and
+// round robin over the final partial pass. Either way the grid as a whole
+// moves through the arrays front to back. The L2-prefetching forms of the
+// double-buffered kernel (fp32 gradient, N <= 6) measured 1-2% faster with
+// adjacent chunks; every other form 1-4% faster round robin.
+struct ChunkMap {
+  int64_t nchunk, pass, full;
+  __device__ explicit ChunkMap(int64_t nvec)
+      : nchunk((nvec + 31) / 32), pass(static_cast<int64_t>(gridDim.x) * kChunkWarps), full(nchunk / pass) {}
+  // The block's j-th chunk; increasing in j, so once a value reaches nchunk
+  // every later one does too.
+  template <bool ADJACENT>
+  __device__ __forceinline__ int64_t chunk(unsigned j) const {
+    if constexpr (ADJACENT) {
+      const int64_t s = j / kChunkWarps;
+      if (s < full) return s * pass + static_cast<int64_t>(blockIdx.x) * kChunkWarps + j % kChunkWarps;
+      return full * pass + (static_cast<int64_t>(j) - full * kChunkWarps) * gridDim.x + blockIdx.x;
+    } else {
+      return static_cast<int64_t>(j) * gridDim.x + blockIdx.x;
+    }
+  }
+  // The calling warp's next chunk from the block's counter (all lanes call;
+  // >= nchunk once the block's chunks are all taken).
+  template <bool ADJACENT>
+  __device__ __forceinline__ int64_t take(unsigned* counter, int lane) const {
+    unsigned j = 0;
+    if (lane == 0) j = atomicAdd(counter, 1u);
+    return chunk<ADJACENT>(__shfl_sync(0xFFFFFFFFu, j, 0));
+  }
+};
+
 // ------------------------------------------------------------------ fused AdamW step
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
@@ -42,63 +86,70 @@ __device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float 
 constexpr int kVecPrefetchRanks = SS_VEC_PF_RANKS;
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
-__global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+__global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) adam_vec_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+  __shared__ unsigned next_chunk;
+  if (threadIdx.x == 0) next_chunk = 0;
+  __syncthreads();
   pdl_wait();
   pdl_trigger();
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  bool bad = false;
-  // moderate rank counts: the warp also asks the L2 for its next groups, one bulk prefetch per
-  // array (lane k takes array k), as the double-buffered kernel does for few ranks
   const int lane = threadIdx.x & 31;
+  const ChunkMap map(nvec);
+  bool bad = false;
+  // moderate rank counts: the warp also asks the L2 for its next chunk, one bulk prefetch per
+  // array (lane k takes array k), as the double-buffered kernel does for few ranks
   const int npf = (!FROM_G32 && a.n_ranks <= kVecPrefetchRanks) ? a.n_ranks + 3 : 0;
-  for (int64_t gi = tid; gi < nvec; gi += stride) {
-    const int64_t e = a.head + gi * kGroup;
-    if (npf) {
-      const int64_t b = (gi - lane) + stride;
-      if (b < nvec && lane < npf) {
-        const int64_t cnt = nvec - b < 32 ? nvec - b : 32;
-        const int64_t eb = a.head + b * kGroup;
-        if (lane < a.n_ranks) {
-          prefetch_l2(static_cast<const uint16_t*>(a.ranks.p[lane]) + eb, static_cast<uint32_t>(cnt * 16));
-        } else {
-          const int k = lane - a.n_ranks;
-          prefetch_l2((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + eb, static_cast<uint32_t>(cnt * 32));
+  int64_t c = map.take<false>(&next_chunk, lane);
+  while (c < map.nchunk) {
+    const int64_t cn = map.take<false>(&next_chunk, lane);
+    if (npf && cn < map.nchunk && lane < npf) {
+      const int64_t b = cn * 32;
+      const int64_t cnt = nvec - b < 32 ? nvec - b : 32;
+      const int64_t eb = a.head + b * kGroup;
+      if (lane < a.n_ranks) {
+        prefetch_l2(static_cast<const uint16_t*>(a.ranks.p[lane]) + eb, static_cast<uint32_t>(cnt * 16));
+      } else {
+        const int k = lane - a.n_ranks;
+        prefetch_l2((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + eb, static_cast<uint32_t>(cnt * 32));
+      }
+    }
+    const int64_t gi = c * 32 + lane;
+    if (gi < nvec) {
+      const int64_t e = a.head + gi * kGroup;
+      float g[8];
+      if constexpr (FROM_G32) {
+        ld8f(a.g32 + e, g);
+      } else {
+        reduce8<GT>(a.ranks, a.n_ranks, e, g);
+        if (a.post_scale != 1.0f) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
         }
       }
-    }
-    float g[8];
-    if constexpr (FROM_G32) {
-      ld8f(a.g32 + e, g);
-    } else {
-      reduce8<GT>(a.ranks, a.n_ranks, e, g);
-      if (a.post_scale != 1.0f) {
+      if (a.nonfinite) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
       }
-    }
-    if (a.nonfinite) {
+      if (a.g_out) st8f(a.g_out + e, g);
+      if (a.dev_scale) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-    }
-    if (a.g_out) st8f(a.g_out + e, g);
-    if (a.dev_scale) {
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+      }
+      float p[8], m[8], v[8];
+      ld8f(a.master + e, p);
+      ld8f(a.m + e, m);
+      ld8f(a.v + e, v);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
+      for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
+      st8f(a.master + e, p);
+      st8f(a.m + e, m);
+      st8f(a.v + e, v);
+      if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
     }
-    float p[8], m[8], v[8];
-    ld8f(a.master + e, p);
-    ld8f(a.m + e, m);
-    ld8f(a.v + e, v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
-    st8f(a.master + e, p);
-    st8f(a.m + e, m);
-    st8f(a.v + e, v);
-    if constexpr (WRITE_P16) __stcs(reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.p16) + e), narrow8<PT>(p));
+    c = cn;
   }
   // the (< 8) elements before the aligned body and the (< 8) after it
   const int64_t tail0 = a.head + nvec * kGroup;
@@ -112,12 +163,12 @@ __global__ void __launch_bounds__(kStepThreads, SS_STEP_MIN_BLOCKS) adam_vec_ker
   }
 }
 
-// Register double-buffered form for small rank counts: the loads of a
-// thread's next group are issued before the update of its current group, so
-// each thread keeps two groups of bytes in flight (for small N, where one
-// group alone is too few bytes to cover HBM latency at the
-// residency the update's registers allow). NR is the rank count; with F the
-// gradient is the fp32 array g32, held as NR = 2 raw 16-byte chunks.
+// Register double-buffered form for small rank counts: the loads of a warp's
+// next chunk are issued before the update of its current one, so each thread
+// keeps two groups of bytes in flight (for small N, where one group alone is
+// too few bytes to cover HBM latency at the residency the update's registers
+// allow). NR is the rank count; with F the gradient is the fp32 array g32,
+// held as NR = 2 raw 16-byte chunks.
 // The rank counts (bit N set: N ranks) that take this form; the others take
 // the single-buffered kernel, which with its L2 prefetch measured faster on
 // GB300 for 5 and 6 ranks at 2^26 elements.
@@ -158,26 +209,8 @@ __device__ __forceinline__ void pipe_load(const StepArgs<MAXR>& a, int64_t gi, P
   G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + e) + 1);
 }
 
-// Work division: a chunk is 32 consecutive groups, one per lane of a warp.
-// Sweep s of the grid covers chunks [s * gridDim.x * W, (s + 1) * gridDim.x * W)
-// with W = warps per block, and block b owns the W chunks at b * W of every
-// sweep (the grid moves through the arrays front to back, as a grid-stride loop
-// would). A block's warps take its chunks in order from a counter in shared
-// memory, so a warp whose loads come back sooner takes more of them and the
-// block's warps finish together. Measured on GB300 (GPT-2 shard, N = 8): with
-// one fixed chunk per warp and sweep, warp finishing times within an SM spread
-// over ~9 us of a ~100 us kernel, with the shared counter over ~3 us; one block
-// of 512 threads per SM (128 registers a thread) lets all 16 warps of an SM
-// share one counter.
-#ifndef SS_PIPE_THREADS
-#define SS_PIPE_THREADS 512
-#endif
-constexpr int kPipeThreads = SS_PIPE_THREADS;
-constexpr int kPipeWarps = kPipeThreads / 32;
-constexpr int kPipeBlocksPerSm = 512 / kPipeThreads;  // at 128 registers a thread
-
 template <int GT, int PT, bool F, bool WRITE_P16, int MAXR, int NR>
-__global__ void __launch_bounds__(kPipeThreads, kPipeBlocksPerSm) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+__global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) adam_pipe_kernel(const __grid_constant__ StepArgs<MAXR> a) {
   __shared__ unsigned next_chunk;
   if (threadIdx.x == 0) next_chunk = 0;
   __syncthreads();
@@ -186,18 +219,12 @@ __global__ void __launch_bounds__(kPipeThreads, kPipeBlocksPerSm) adam_pipe_kern
   if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
   const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
   const int64_t nvec = (a.n - a.head) / kGroup;
-  const int64_t nchunk = (nvec + 31) / 32;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t per_sweep = static_cast<int64_t>(gridDim.x) * kPipeWarps;
   const int lane = threadIdx.x & 31;
-  // the warp's next chunk (>= nchunk once the block's chunks are all taken)
-  auto take = [&]() -> int64_t {
-    unsigned j = 0;
-    if (lane == 0) j = atomicAdd(&next_chunk, 1u);
-    j = __shfl_sync(0xFFFFFFFFu, j, 0);
-    return static_cast<int64_t>(j / kPipeWarps) * per_sweep + static_cast<int64_t>(blockIdx.x) * kPipeWarps +
-           (j % kPipeWarps);
-  };
+  constexpr bool kPrefetch = F || NR <= kPipePrefetchRanks;
+  const ChunkMap map(nvec);
+  const int64_t nchunk = map.nchunk;
+  auto take = [&]() -> int64_t { return map.take<kPrefetch>(&next_chunk, lane); };
   bool bad = false;
   PipeGroup<NR> cur, nxt;
   int64_t c = take();
@@ -206,7 +233,7 @@ __global__ void __launch_bounds__(kPipeThreads, kPipeBlocksPerSm) adam_pipe_kern
   while (c < nchunk) {
     const int64_t cnn = cn < nchunk ? take() : nchunk;
     if (cn < nchunk && cn * 32 + lane < nvec) pipe_load<GT, NR, F>(a, cn * 32 + lane, nxt);
-    if constexpr (F || NR <= kPipePrefetchRanks) {
+    if constexpr (kPrefetch) {
       // L2 prefetch of the warp's chunk after next, one bulk prefetch per array (lane k takes
       // array k): more bytes in flight without registers, for groups whose own loads are few.
       // Hints only; every range lies inside its array.
@@ -615,8 +642,8 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
 template <int G, int P, bool W, int MAXR, int NR, bool F = false>
 ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
   auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
-  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kPipeThreads), a, stream,
-                kPipeThreads);
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kChunkThreads), a, stream,
+                kChunkThreads);
 }
 
 template <int G, int P, bool W, int MAXR>
@@ -652,8 +679,8 @@ ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, 
       if constexpr (F) return SS_ERR_INVALID_ARG;                                         \
       else {                                                                              \
         auto* fn = adam_vec_kernel<G, P, F, W, MAXR>;                                     \
-        return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kStepThreads), a, \
-                      stream, kStepThreads);                                              \
+        return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kChunkThreads), a, \
+                      stream, kChunkThreads);                                             \
       }                                                                                   \
     }                                                                                     \
     auto* fn = adam_scalar_kernel<G, P, F, W, MAXR>;                                      \
