@@ -17,15 +17,29 @@ __device__ __forceinline__ void reduce_one(const ReduceArgs<MAXR>& a, int64_t e,
   a.out[e] = g;
 }
 
-template <int GT, int MAXR>
-__global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+// With CHUNKED (up to kReduceChunkRanks ranks) one block of 1024 threads per SM
+// whose warps take chunks of 32 groups from a shared counter (ChunkMap, round
+// robin); otherwise a grid-stride loop at 4 blocks of 256 threads per SM.
+// Measured on GB300 at 2^26 elements, chunked against grid-stride: +3.5% at
+// N = 1, +1.8% at N = 2, +8% at N = 4, +0.4% at N = 8 (+2.2% accumulating),
+// -1.5% at N = 64.
+constexpr int kReduceChunkThreads = 1024;
+constexpr int kReduceChunkRanks = 8;
+
+template <int GT, int MAXR, bool CHUNKED>
+__global__ void __launch_bounds__(CHUNKED ? kReduceChunkThreads : kThreads) reduce_vec_kernel(
+    const __grid_constant__ ReduceArgs<MAXR> a) {
+  __shared__ unsigned next_chunk;
+  if constexpr (CHUNKED) {
+    if (threadIdx.x == 0) next_chunk = 0;
+    __syncthreads();
+  }
   pdl_wait();
   pdl_trigger();
   const int64_t nvec = (a.n - a.head) / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   bool bad = false;
-  for (int64_t gi = tid; gi < nvec; gi += stride) {
+  auto group = [&](int64_t gi) {
     const int64_t e = a.head + gi * kGroup;
     float g[8];
     reduce8<GT>(a.ranks, a.n_ranks, e, g);
@@ -44,6 +58,17 @@ __global__ void __launch_bounds__(kThreads) reduce_vec_kernel(const __grid_const
       for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
     }
     st8f(a.out + e, g);
+  };
+  if constexpr (CHUNKED) {
+    const ChunkMap<kReduceChunkThreads / 32> map(nvec);
+    const int lane = threadIdx.x & 31;
+    for (int64_t c = map.take<false>(&next_chunk, lane); c < map.nchunk; c = map.take<false>(&next_chunk, lane)) {
+      const int64_t gi = c * 32 + lane;
+      if (gi < nvec) group(gi);
+    }
+  } else {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t gi = tid; gi < nvec; gi += stride) group(gi);
   }
   const int64_t tail0 = a.head + nvec * kGroup;
   if (tid < a.head + (a.n - tail0)) reduce_one<GT>(a, tid < a.head ? tid : tail0 + (tid - a.head), bad);
@@ -71,8 +96,13 @@ template <int MAXR>
 ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* stream) {
 #define SS_RED_CASE(G)                                                                     \
   if (gt == G) {                                                                           \
+    if (vec && a.n_ranks <= kReduceChunkRanks) {                                           \
+      auto* fn = reduce_vec_kernel<G, MAXR, true>;                                         \
+      return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kReduceChunkThreads), \
+                    a, stream, kReduceChunkThreads);                                       \
+    }                                                                                      \
     if (vec) {                                                                             \
-      auto* fn = reduce_vec_kernel<G, MAXR>;                                               \
+      auto* fn = reduce_vec_kernel<G, MAXR, false>;                                        \
       return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), a, stream); \
     }                                                                                      \
     auto* fn = reduce_scalar_kernel<G, MAXR>;                                              \

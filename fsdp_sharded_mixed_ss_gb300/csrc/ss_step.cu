@@ -11,50 +11,6 @@
 namespace ss {
 namespace {
 
-// ------------------------------------------------------------------ work division
-//
-// The vector and double-buffered step kernels run one wave of blocks, one per
-// SM. A chunk is 32 consecutive 8-element groups, one per lane of a warp; each
-// block owns a fixed set of chunks and its warps take them in order from a
-// counter in shared memory, so a warp whose loads come back sooner takes more
-// of them and the 16 warps of an SM finish together. Measured on GB300 (GPT-2
-// shard, N = 8, per-warp timer stamps in a probe build): with one fixed chunk
-// per warp and pass over the grid the warps of an SM finished up to ~9 us
-// apart in a ~100 us launch, with the counter within ~3 us.
-//
-// Which chunks block b of B owns: round robin, chunks b, b + B, b + 2B, ...
-// (the blocks' counts differ by at most one); or ADJACENT: W adjacent chunks
-// (W = warps per block) of every full pass of the grid over W * B chunks, and
-// round robin over the final partial pass. Either way the grid as a whole
-// moves through the arrays front to back. The L2-prefetching forms of the
-// double-buffered kernel (fp32 gradient, N <= 6) measured 1-2% faster with
-// adjacent chunks; every other form 1-4% faster round robin.
-struct ChunkMap {
-  int64_t nchunk, pass, full;
-  __device__ explicit ChunkMap(int64_t nvec)
-      : nchunk((nvec + 31) / 32), pass(static_cast<int64_t>(gridDim.x) * kChunkWarps), full(nchunk / pass) {}
-  // The block's j-th chunk; increasing in j, so once a value reaches nchunk
-  // every later one does too.
-  template <bool ADJACENT>
-  __device__ __forceinline__ int64_t chunk(unsigned j) const {
-    if constexpr (ADJACENT) {
-      const int64_t s = j / kChunkWarps;
-      if (s < full) return s * pass + static_cast<int64_t>(blockIdx.x) * kChunkWarps + j % kChunkWarps;
-      return full * pass + (static_cast<int64_t>(j) - full * kChunkWarps) * gridDim.x + blockIdx.x;
-    } else {
-      return static_cast<int64_t>(j) * gridDim.x + blockIdx.x;
-    }
-  }
-  // The calling warp's next chunk from the block's counter (all lanes call;
-  // >= nchunk once the block's chunks are all taken).
-  template <bool ADJACENT>
-  __device__ __forceinline__ int64_t take(unsigned* counter, int lane) const {
-    unsigned j = 0;
-    if (lane == 0) j = atomicAdd(counter, 1u);
-    return chunk<ADJACENT>(__shfl_sync(0xFFFFFFFFu, j, 0));
-  }
-};
-
 // ------------------------------------------------------------------ fused AdamW step
 
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
@@ -97,7 +53,7 @@ __global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) adam_vec_ker
   const int64_t nvec = (a.n - a.head) / kGroup;
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
-  const ChunkMap map(nvec);
+  const ChunkMap<kChunkWarps> map(nvec);
   bool bad = false;
   // moderate rank counts: the warp also asks the L2 for its next chunk, one bulk prefetch per
   // array (lane k takes array k), as the double-buffered kernel does for few ranks
@@ -222,7 +178,7 @@ __global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) adam_pipe_ke
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   constexpr bool kPrefetch = F || NR <= kPipePrefetchRanks;
-  const ChunkMap map(nvec);
+  const ChunkMap<kChunkWarps> map(nvec);
   const int64_t nchunk = map.nchunk;
   auto take = [&]() -> int64_t { return map.take<kPrefetch>(&next_chunk, lane); };
   bool bad = false;
