@@ -65,18 +65,23 @@ def measured_peaks() -> dict:
 
 
 def kernel_fingerprint() -> str:
-    """SHA-256 of the fused step kernel's source: the per-element arithmetic header and the
-    double-buffered kernel's text in the CUDA source (from its comment block to the next kernel)."""
+    """SHA-256 of the fused step kernel's source: the per-element arithmetic header, the work
+    division it takes its chunks from (the common header's section) and the double-buffered
+    kernel's text in the CUDA source (from its comment block to the next kernel)."""
     import hashlib
 
     src = os.path.join(ROOT, "fsdp_sharded_mixed_ss_gb300", "csrc")
     with open(os.path.join(src, "ss_math.cuh"), "rb") as f:
         math = f.read()
+    with open(os.path.join(src, "ss_common.cuh")) as f:
+        common = f.read()
     with open(os.path.join(src, "ss_step.cu")) as f:
         text = f.read()
+    c0 = common.index("// ------------------------------------------------------------------ work division")
+    c1 = common.index("// Programmatic dependent launch", c0)
     start = text.index("// Register double-buffered form for small rank counts")
     end = text.index("adam_scalar_kernel(", start)
-    return hashlib.sha256(math + text[start:end].encode()).hexdigest()
+    return hashlib.sha256(math + common[c0:c1].encode() + text[start:end].encode()).hexdigest()
 
 
 def profile_traffic(kernel: str):
