@@ -189,6 +189,51 @@ def test_step_gradient_and_param_formats(ss, gfmt, pfmt, N, goff):
     _check(master, m, v, p16, (None, g, master0, m0, v0, rp), pfmt)
 
 
+def _sms():
+    import torch
+    return torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("N,from_g32", [(1, False), (2, True), (5, False), (8, False)])
+@pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, -2049), (2, 255), (3, 4103)])
+def test_step_chunk_boundaries(ss, N, from_g32, k, d):
+    """Shard lengths around whole passes of the grid over its chunks (a pass: 16 chunks of 32
+    8-element groups per block, one block per SM), so the last pass is just full, just short or
+    just over, through each way the step kernels own chunks: adjacent per block (1 rank, an fp32
+    gradient), round robin (5 ranks: single-buffered kernel; 8 ranks: double-buffered). Every
+    element is stepped exactly once: all of the state against the oracle."""
+    import torch
+    n = k * _sms() * 16 * 32 * 8 + d
+    ref = _oracle_step(n, N, synth.BF16, HP)
+    master, m, v = _state(n)
+    p16 = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    if from_g32:
+        g32 = torch.from_numpy(np.ascontiguousarray(ref[1], dtype=np.float32)).cuda()
+        ss.ss_adam_step(HP, n, master, m, v, g32=g32, param16=p16)
+    else:
+        G = [dev_bits(s, n) for s in ref[0]]
+        ss.ss_adam_step(HP, n, master, m, v, rank_grads=G, param16=p16)
+    _check(master, m, v, p16, ref, synth.BF16)
+
+
+@pytest.mark.parametrize("N", [1, 4, 8, 9])
+@pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (2, 257), (3, -4096)])
+def test_reduce_chunk_boundaries(ss, N, k, d):
+    """The reduce around whole passes of its grid (32 chunks of 256 elements per block, one block
+    per SM) for the chunked form (up to 8 ranks) and the grid-stride one (9), accumulating into
+    the output: bit-exact, so no element is added twice or missed."""
+    import torch
+    n = k * _sms() * 32 * 32 * 8 + d
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 4) for r in range(N)]
+    G = [dev_bits(s, n) for s in specs]
+    init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
+    out = init.clone()
+    ss.ss_grad_reduce(G, n, out, accumulate=True)
+    acc = bits_of(init).copy()
+    oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, accumulate_into=acc)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+
+
 def test_step_from_fp32_grad_matches_fused(ss):
     import torch
     n, N = 50_001, 8
