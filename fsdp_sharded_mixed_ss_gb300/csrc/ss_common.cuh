@@ -14,7 +14,10 @@
 //     rank gradient (8 x 16-bit), two 16-byte loads per fp32 state array;
 //     every access is a full 16-byte vector, so each warp moves 512 bytes of
 //     each array per instruction, fully coalesced;
-//   * persistent grid (SM count x resident blocks), grid-stride loop;
+//   * persistent grid, one wave (SM count x resident blocks); the fused step
+//     and the reduce of up to 8 ranks run one block per SM whose warps take
+//     chunks of 32 groups from a shared-memory counter (work division below),
+//     the other kernels a grid-stride loop;
 //   * rank gradients are summed in rank order in batches of 8 loads issued
 //     before the adds (8 x 16 B in flight per thread for any N);
 //   * streaming cache hints (evict-first) on read-once and write-once data;
