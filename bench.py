@@ -27,6 +27,7 @@ import argparse
 import json
 import os
 import statistics
+import re
 import subprocess
 import sys
 import threading
@@ -50,6 +51,8 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="instead of the benchmark line, time every kernel on the sweep and layer shapes")
     ap.add_argument("--suite-n", type=int, default=1 << 26, help="shard length of the --suite runs")
+    ap.add_argument("--suite-only", default=None, metavar="REGEX",
+                    help="time only the --suite entries whose name matches (e.g. for a small ncu capture)")
     return ap.parse_args()
 
 
@@ -442,6 +445,9 @@ def run_suite(args, device) -> dict:
     def entry(ms, nbytes):
         return {"ms": round(ms, 4), "GB/s": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
+    def want(*names):
+        return args.suite_only is None or any(re.search(args.suite_only, k) for k in names)
+
     out = {"peak_hbm_gbs": measured_peaks()["hbm_gbs"], "n": args.suite_n}
     n = args.suite_n
     hp = dict(lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1000)
@@ -454,81 +460,100 @@ def run_suite(args, device) -> dict:
     p16 = torch.empty(n, dtype=torch.bfloat16, device=device)
     g32 = torch.empty(n, dtype=torch.float32, device=device)
     synth.device_fill(synth.normal(1e-3, synth.FP32, synth.GRAD, 0, 1), g32.view(torch.int32))
-    out["adam_step_fp32_grad"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, g32=g32, param16=p16)), 30 * n)
+    if want("adam_step_fp32_grad"):
+        out["adam_step_fp32_grad"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, g32=g32, param16=p16)), 30 * n)
     ws = torch.empty(max(ss.ss_grad_sumsq_workspace(n) // 8, 1), dtype=torch.float64, device=device)
     acc = torch.empty(1, dtype=torch.float64, device=device)
+    extra8 = ("adam_step_N8_grads_off_by_one", "grad_reduce_accumulate_N8", "adam_step_N8_fp16_unscale_flag_skip",
+              "adam_step_N8_param16_into_flat")
     for N in (2, 8, 64):
+        if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", *(extra8 if N == 8 else ())):
+            continue
         G = []
         for r in range(N):
             t = torch.empty(n, dtype=torch.bfloat16, device=device)
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
             G.append(t)
-        out[f"adam_step_N{N}"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=p16)),
-                                       (2 * N + 26) * n)
-        out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
-        out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
-        if N == 8:
+        if want(f"adam_step_N{N}"):
+            out[f"adam_step_N{N}"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=p16)),
+                                           (2 * N + 26) * n)
+        if want(f"grad_reduce_N{N}"):
+            out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
+        if want(f"grad_sumsq_N{N}"):
+            out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
+        if N == 8 and want(extra8[0]):
             # gradient views one element off the state's 16-byte phase: the shifted-load kernels
             Gm = [g[1:] for g in G]
             m1 = n - 1
-            out["adam_step_N8_grads_off_by_one"] = entry(
+            out[extra8[0]] = entry(
                 timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1]), 5),
                 (2 * N + 26) * m1)
+        if N == 8 and want(extra8[1]):
             # next rows: gradient accumulation (read-modify-write of the fp32 gradient) ...
-            out["grad_reduce_accumulate_N8"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32, accumulate=True)),
-                                                     (2 * N + 8) * n)
+            out[extra8[1]] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32, accumulate=True)), (2 * N + 8) * n)
+        if N == 8 and want(extra8[2]):
             # ... fp16 loss-scale unscaling with the overflow flag and the skip flag read ...
             G16 = [g.view(torch.float16) for g in G]   # the same bits read as fp16: finite, small
             flag = torch.zeros(2, dtype=torch.int32, device=device)   # [0]: this step's flag, [1]: skip
-            out["adam_step_N8_fp16_unscale_flag_skip"] = entry(
+            out[extra8[2]] = entry(
                 timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G16, post_scale=1.0 / 1024, param16=p16,
                                               nonfinite_flag=flag[0:1], dev_skip_flag=flag[1:2])), (2 * N + 26) * n)
             assert int(flag[0].item()) == 0
+            del flag
+        if N == 8 and want(extra8[3]):
             # ... and the 16-bit parameters written straight into a flat unit buffer at the shard's offset
             flat = torch.empty(n + 1024, dtype=torch.bfloat16, device=device)
-            out["adam_step_N8_param16_into_flat"] = entry(
+            out[extra8[3]] = entry(
                 timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=flat[1024:])), (2 * N + 26) * n)
-            del flat, flag
+            del flat
         del G
         torch.cuda.empty_cache()
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
-    G = []
-    for r in range(32):
-        t = torch.empty(n, dtype=torch.bfloat16, device=device)
-        synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
-        G.append(t)
-    by_ranks = {}
-    for N in (1, 3, 4, 5, 6, 7, 9, 10, 12, 13, 16, 24, 32):
-        Gn = G[:N]
-        by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=Gn, param16=p16)),
-                                 (2 * N + 26) * n)
-    out["adam_step_by_ranks"] = by_ranks
-    del G
+    if want("adam_step_by_ranks"):
+        G = []
+        for r in range(32):
+            t = torch.empty(n, dtype=torch.bfloat16, device=device)
+            synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+            G.append(t)
+        by_ranks = {}
+        for N in (1, 3, 4, 5, 6, 7, 9, 10, 12, 13, 16, 24, 32):
+            Gn = G[:N]
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=Gn, param16=p16)),
+                                     (2 * N + 26) * n)
+        out["adam_step_by_ranks"] = by_ranks
+        del G
     del st, p16, g32, ws
     torch.cuda.empty_cache()
-    out.update(run_config_steps(ss, device, timed, entry))
+    out.update(run_config_steps(ss, device, timed, entry, want))
     for name, numels, N, dt in (("unshard_gpt2_small_N8", [124_439_808], 8, torch.bfloat16),
                                 ("unshard_llama70b_layer_N64", [855_654_400], 64, torch.float16)):
+        reshard = name.replace("unshard", "reshard")
+        off_names = (name + "_flat_off_phase", reshard + "_flat_off_phase") if N == 8 else ()
+        if not want(name, reshard, *off_names):
+            continue
         _, b = ss.ss_flatten_layout(numels, N)
         P = int(b[-1])
         shards = [torch.zeros(int(b[k + 1] - b[k]), dtype=dt, device=device) for k in range(N)]
         flat = torch.empty(P, dtype=dt, device=device)
-        out[name] = entry(timed(lambda: ss.ss_unshard(shards, b, flat)), 4 * P)
-        out[name.replace("unshard", "reshard")] = entry(timed(lambda: ss.ss_reshard(flat, b, shards)), 4 * P)
-        if N == 8:
+        if want(name):
+            out[name] = entry(timed(lambda: ss.ss_unshard(shards, b, flat)), 4 * P)
+        if want(reshard):
+            out[reshard] = entry(timed(lambda: ss.ss_reshard(flat, b, shards)), 4 * P)
+        if off_names and want(*off_names):
             # flat buffer one element off the shards' 16-byte phase: the SIMT copy with shifted loads
             base = torch.empty(P + 8, dtype=dt, device=device)
             off = base[1:P + 1]
-            out[name + "_flat_off_phase"] = entry(timed(lambda: ss.ss_unshard(shards, b, off)), 4 * P)
-            out[name.replace("unshard", "reshard") + "_flat_off_phase"] = entry(
-                timed(lambda: ss.ss_reshard(off, b, shards)), 4 * P)
+            if want(off_names[0]):
+                out[off_names[0]] = entry(timed(lambda: ss.ss_unshard(shards, b, off)), 4 * P)
+            if want(off_names[1]):
+                out[off_names[1]] = entry(timed(lambda: ss.ss_reshard(off, b, shards)), 4 * P)
             del base, off
         del shards, flat
         torch.cuda.empty_cache()
     return out
 
 
-def run_config_steps(ss, device, timed, entry) -> dict:
+def run_config_steps(ss, device, timed, entry, want=lambda *names: True) -> dict:
     """The two large configurations at full size: the Llama-3-8B rank-0 shard (1,003,782,656
     elements, 8 bf16 ranks with outliers) and the Llama-70B layer stepped as one unit (855,654,400
     elements, 64 fp16 ranks, every shard at once, parameters written straight into the flat
@@ -540,6 +565,9 @@ def run_config_steps(ss, device, timed, entry) -> dict:
 
     out = {}
     for w, whole_unit in ((workloads.llama3_8b_shard(), False), (workloads.llama70b_layer(), True)):
+        key = f"{w.name}_{'unit_step_into_flat' if whole_unit else 'shard_step'}"
+        if not want(key):
+            continue
         _, b = ss.ss_flatten_layout(w.numels, w.n_ranks)
         n = int(b[-1]) if whole_unit else int(b[1])
         dt = torch.bfloat16 if w.gdtype == synth.BF16 else torch.float16
@@ -553,7 +581,6 @@ def run_config_steps(ss, device, timed, entry) -> dict:
         st += [torch.zeros(n, dtype=torch.float32, device=device) for _ in range(2)]
         p16 = torch.empty(n, dtype=dt, device=device)
         hp = w.hp(1)
-        key = f"{w.name}_{'unit_step_into_flat' if whole_unit else 'shard_step'}"
         out[key] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, rank_grads=G, param16=p16), 5),
                          (2 * w.n_ranks + 26) * n)
         out[key]["elements"] = n
