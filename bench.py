@@ -1,17 +1,21 @@
 #!/usr/bin/env python3
 """Benchmark of the fused shard step on GB300.
 
-Workload (one "step" = one pass of the whole hot path): the GPT-2 small unit
-(124,439,808 parameters in 148 tensors) flattened and cut into N = 8
-virtual-rank shards; rank 0's shard (15,554,976 elements) runs the fused
-reduce of the 8 ranks' bf16 gradients + AdamW on fp32 master/m/v + bf16 cast
-in one kernel, then the unshard copy gathers the 8 bf16 shards into the flat
-unit buffer. Inputs are synthetic (seeded generator) and resident in HBM;
-one step moves 1.15 GB, far above the 129 MB L2, so no L2 flush is needed.
+Workload (one "step" = one pass of the whole hot path): the Llama-3-8B unit
+(8,030,261,248 parameters in 291 tensors, module order) flattened and cut at
+floor(kP/8) into N = 8 virtual-rank shards of 1,003,782,656 elements. Rank 0's
+shard runs the fused kernel -- the rank-ordered fp32 sum of the 8 ranks' bf16
+gradients (N(0, 1e-4) with 1% of entries x100), AdamW on fp32 master/m/v and
+the bf16 cast -- then the unshard copy gathers the 8 bf16 shards into the flat
+unit buffer. Inputs are synthetic (seeded generator) and resident in HBM; one
+step moves 74.3 GB, far above the 129 MB L2, so no L2 flush is needed.
 
 Metric: algorithmic HBM bytes of the step / step time (GB/s), with params/s
-(shard elements updated per second) and the dominant kernel's roofline
-fraction against the measured HBM copy bandwidth.
+(shard elements updated per second). Each kernel is also timed alone, back to
+back, and reported with its roofline fraction against the measured HBM copy
+bandwidth; the two per-kernel times must add up to the step time. Secondary
+blocks time the GPT-2 small rank-0 shard step + unshard and the Llama-70B layer
+(64 fp16 shard steps + unshard + reshard) the same way.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -37,16 +41,19 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused shard-step HBM GB/s and params/s (fraction of GB300 HBM peak), 1 GPU"
-WORKLOAD = "gpt2-small-124M flat unit, N=8 virtual ranks: rank-0 shard fused reduce+AdamW+bf16 cast, then full unshard"
+WORKLOAD = ("llama3-8b flat unit (8,030,261,248 params), N=8 virtual ranks: rank-0 shard (1,003,782,656 elements) "
+            "fused reduce of 8 bf16 grads + AdamW + bf16 cast, then unshard of the 8 bf16 shards into the flat unit")
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg (e.g. under a profiler)")
+    ap.add_argument("--no-secondary", action="store_true", help="skip the GPT-2 and Llama-70B layer blocks")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="instead of the benchmark line, time every kernel on the sweep and layer shapes")
@@ -87,8 +94,9 @@ def kernel_fingerprint() -> str:
     return hashlib.sha256(math + common[c0:c1].encode() + text[start:end].encode()).hexdigest()
 
 
-def profile_traffic(kernel: str):
-    """DRAM bytes per launch from the committed ncu summary, while the kernel's source still matches it."""
+def profile_traffic(kernel: str, elements: int):
+    """DRAM bytes per launch from the committed ncu record, while the record is for this kernel
+    on a shard of this many elements and the kernel's source still matches it."""
     path = os.path.join(ROOT, "profiles", "adam_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -98,7 +106,7 @@ def profile_traffic(kernel: str):
             if "=" in line and not line.lstrip().startswith("#"):
                 k, v = line.split("=", 1)
                 ent[k.strip()] = v.strip()
-    if ent.get("kernel") != kernel:
+    if ent.get("kernel") != kernel or ent.get("elements") != str(elements):
         return None
     if ent.get("source_sha256") != kernel_fingerprint():
         return None                     # the kernel changed since the counters were taken
@@ -136,7 +144,7 @@ class ClockSampler:
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", self._smi_id(), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -183,41 +191,56 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def setup(device):
+def unit_setup(w, device, stepped, state_whole_unit: bool = False):
+    """Device buffers of one unit: the ranks' 16-bit gradients, fp32 master/m/v of the stepped
+    shards, every shard's 16-bit parameters and the flat unit buffer, all from seeded streams.
+    Gradients hold the full unit per rank when `w.per_rank_full`, else rank 0's shard only;
+    with `state_whole_unit` master/m/v are unit-wide arrays viewed per shard."""
     import torch
 
     import fsdp_sharded_mixed_ss_gb300 as ss
     import synth
-    from synth import workloads
 
-    w = workloads.gpt2_small()
     N, P = w.n_ranks, w.P
-    offs, bounds = ss.ss_flatten_layout(w.numels, N)
-    n = int(bounds[1] - bounds[0])
-    G = [torch.empty(P, dtype=torch.bfloat16, device=device) for _ in range(N)]
+    _, bounds = ss.ss_flatten_layout(w.numels, N)
+    bounds = [int(x) for x in bounds]
+    dt = torch.bfloat16 if w.gdtype == synth.BF16 else torch.float16
+    glen = P if w.per_rank_full else bounds[1]
+    grads = torch.empty((N, glen), dtype=dt, device=device)
     for r in range(N):
-        synth.device_fill(w.grad(r, 1), G[r].view(torch.int16))
-    master = torch.empty(n, dtype=torch.float32, device=device)
-    synth.device_fill(w.master, master.view(torch.int32))
-    m = torch.zeros(n, dtype=torch.float32, device=device)
-    v = torch.zeros(n, dtype=torch.float32, device=device)
+        synth.device_fill(w.grad(r, 1), grads[r].view(torch.int16))
+    lo_all, hi_all = (0, P) if state_whole_unit else (bounds[stepped[0]], bounds[stepped[-1] + 1])
+    st = []
+    for i in range(3):
+        t = torch.zeros(hi_all - lo_all, dtype=torch.float32, device=device)
+        if i == 0:
+            synth.device_fill(w.master, t.view(torch.int32), start=lo_all)
+        st.append(t)
     shards = []
     for k in range(N):
-        lo, hi = int(bounds[k]), int(bounds[k + 1])
-        t = torch.empty(hi - lo, dtype=torch.bfloat16, device=device)
-        synth.device_fill(w.param16(k), t.view(torch.int16), start=lo)
+        t = torch.empty(bounds[k + 1] - bounds[k], dtype=dt, device=device)
+        synth.device_fill(w.param16(k) if w.param16 is not None else synth.normal(0.02, w.gdtype, synth.PARAM16, k),
+                          t.view(torch.int16), start=bounds[k])
         shards.append(t)
-    flat = torch.empty(P, dtype=torch.bfloat16, device=device)
-    views = [g[:n] for g in G]
+    flat = torch.empty(P, dtype=dt, device=device)
     torch.cuda.synchronize(device)
-    return dict(ss=ss, w=w, N=N, P=P, n=n, bounds=bounds, G=G, views=views, master=master, m=m, v=v,
-                shards=shards, flat=flat)
+
+    def shard_args(k):
+        lo, hi = bounds[k], bounds[k + 1]
+        views = [grads[r, lo:hi] for r in range(N)] if w.per_rank_full else [grads[r] for r in range(N)]
+        return hi - lo, [x[lo - lo_all:hi - lo_all] for x in st], views
+
+    return dict(w=w, N=N, P=P, bounds=bounds, grads=grads, state=st, shards=shards, flat=flat,
+                stepped=list(stepped), shard_args=shard_args)
 
 
-def bytes_per_step(s) -> tuple[int, int]:
-    adam = s["n"] * (2 * s["N"] + 26)          # N x 2 B grads read, 12 B state read, 12 B written, 2 B param written
-    unshard = 4 * s["P"]                        # 2 B read + 2 B written per element of the unit
-    return adam, unshard
+def step_bytes(u) -> dict:
+    """Algorithmic bytes of one step: the fused kernel reads N x 2 B of gradients and 12 B of state
+    and writes 12 B of state and 2 B of parameters per shard element; a copy moves 2 B in and 2 B
+    out per element of the unit."""
+    N, b = u["N"], u["bounds"]
+    adam = sum((b[k + 1] - b[k]) * (2 * N + 26) for k in u["stepped"])
+    return {"adam": adam, "copy": 4 * u["P"]}
 
 
 def max_over_ranks(values, device=None):
@@ -238,58 +261,97 @@ def job_gbs(bytes_per_rank_step: int, world: int, ms_per_step: float) -> float:
     return bytes_per_rank_step * world / (ms_per_step * 1e-3) / 1e9
 
 
-def run_e2e(s, steps: int, device, t_counter, readback: str = "flag"):
-    """Steps through the public API with the gradients copied in from pinned host memory every
-    step, and every step's result read back to the host: readback="flag" reads the step's
-    non-finite-gradient flag (4 bytes, the found-inf value a mixed-precision loop reads each step),
-    readback="params" the whole flat bf16 unit. Three streams: the host-to-device copy of step i+1
-    and the device-to-host copy of step i-1 overlap step i (double-buffered device inputs and
-    outputs). Returns (ms per step, H2D GB/s alone, D2H GB/s alone)."""
+def timed_block(fn, reps: int, stream) -> float:
+    """Mean ms of `reps` back-to-back calls of fn, between two CUDA events on `stream` (the
+    stream every call launches on), synchronised on both sides."""
     import torch
 
-    ss, w = s["ss"], s["w"]
-    n, N, P = s["n"], s["N"], s["P"]
-    host_in = torch.empty((N, n), dtype=torch.bfloat16, pin_memory=True)
-    for r in range(N):
-        host_in[r].copy_(s["views"][r])
-    dev_in = [torch.empty((N, n), dtype=torch.bfloat16, device=device) for _ in range(2)]
-    flat = [s["flat"], torch.empty(P, dtype=torch.bfloat16, device=device)]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def kernel_split(parts: dict, step_ms: float, peak: float) -> dict:
+    """Per-kernel timings of a step (each kernel timed alone, back to back) with their GB/s and
+    fractions of the copy peak, and the check that they add up to the step's own time."""
+    out = {}
+    total = 0.0
+    for name, (ms, nbytes, launches) in parts.items():
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[name] = {"ms_per_step": round(ms, 5), "launches_per_step": launches,
+                     "avg_launch_ms": round(ms / launches, 5), "bytes_per_step": nbytes,
+                     "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4)}
+        total += ms
+    out["sum_check"] = {"sum_ms": round(total, 5), "step_ms": round(step_ms, 5),
+                        "ratio": round(total / step_ms, 4), "within_5pct": abs(total / step_ms - 1.0) <= 0.05}
+    return out
+
+
+def run_step_loop(step, steps: int, warmup: int, stream):
+    """W untimed steps, then the mean ms of K steps between two events."""
+    import torch
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    return timed_block(step, steps, stream)
+
+
+def run_e2e(u, steps: int, device, t_counter):
+    """Steps through the public API with every step's gradients copied in from pinned host memory
+    and the step's result -- the fused step's non-finite-gradient flag, the found-inf value a
+    mixed-precision loop reads each step -- read back to the host. Three streams: the host-to-
+    device copy of step i+1 and the device-to-host copy of step i-1 overlap step i (double-
+    buffered device gradients). Returns (ms per step, H2D GB/s alone, input bytes per step)."""
+    import torch
+
+    import fsdp_sharded_mixed_ss_gb300 as ss
+
+    w, N, b = u["w"], u["N"], u["bounds"]
+    n = b[1] - b[0]
+    src = u["grads"][:, :n]
+    host_in = torch.empty((N, n), dtype=src.dtype, pin_memory=True)
+    nbytes = host_in.numel() * host_in.element_size()
+    host_in.copy_(src)
+    dev_in = [src.contiguous() if u["w"].per_rank_full else u["grads"],
+              torch.empty((N, n), dtype=src.dtype, device=device)]
     flags = [torch.zeros(1, dtype=torch.int32, device=device) for _ in range(2)]
-    if readback == "params":
-        host_out = [torch.empty(P, dtype=torch.bfloat16, pin_memory=True) for _ in range(2)]
-        dev_out = flat
-    else:
-        host_out = [torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
-        dev_out = flags
+    host_out = [torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(3))
     done = {"h2d": {}, "cmp": {}, "d2h": {}}
+    n0, st, _ = u["shard_args"](0)
 
-    def mark(kind, i, st):
+    def mark(kind, i, s):
         e = torch.cuda.Event()
-        e.record(st)
+        e.record(s)
         done[kind][i] = e
 
     def step(i):
-        b = i % 2
+        j = i % 2
         t = t_counter[0]
         t_counter[0] += 1
         if i - 2 in done["cmp"]:
-            s_h2d.wait_event(done["cmp"][i - 2])          # dev_in[b] no longer read
+            s_h2d.wait_event(done["cmp"][i - 2])          # dev_in[j] no longer read
         with torch.cuda.stream(s_h2d):
-            dev_in[b].copy_(host_in, non_blocking=True)
+            dev_in[j].copy_(host_in, non_blocking=True)
         mark("h2d", i, s_h2d)
         s_cmp.wait_event(done["h2d"][i])
         if i - 2 in done["d2h"]:
-            s_cmp.wait_event(done["d2h"][i - 2])          # dev_out[b] already copied out
+            s_cmp.wait_event(done["d2h"][i - 2])          # flags[j] already copied out
         with torch.cuda.stream(s_cmp):
-            flags[b].zero_()
-        ss.ss_adam_step(w.hp(t), n, s["master"], s["m"], s["v"], rank_grads=[dev_in[b][r] for r in range(N)],
-                        param16=s["shards"][0], nonfinite_flag=flags[b], stream=s_cmp)
-        ss.ss_unshard(s["shards"], s["bounds"], flat[b], stream=s_cmp)
+            flags[j].zero_()
+        ss.ss_adam_step(w.hp(t), n0, *st, rank_grads=[dev_in[j][r] for r in range(N)],
+                        param16=u["shards"][0], nonfinite_flag=flags[j], stream=s_cmp)
+        ss.ss_unshard(u["shards"], b, u["flat"], stream=s_cmp)
         mark("cmp", i, s_cmp)
         s_d2h.wait_event(done["cmp"][i])
         with torch.cuda.stream(s_d2h):
-            host_out[b].copy_(dev_out[b], non_blocking=True)
+            host_out[j].copy_(flags[j], non_blocking=True)
         mark("d2h", i, s_d2h)
 
     for i in range(3):
@@ -306,116 +368,169 @@ def run_e2e(s, steps: int, device, t_counter, readback: str = "flag"):
     e1.record(s_d2h)
     torch.cuda.synchronize(device)
     e2e_ms = e0.elapsed_time(e1) / steps
-
-    # each copy direction alone, for reference
-    def timed(fn):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        st = torch.cuda.current_stream(device)
-        a.record(st)
-        for _ in range(5):
-            fn()
-        b.record(st)
-        torch.cuda.synchronize(device)
-        return a.elapsed_time(b) / 5
-
-    if readback == "flag" and any(int(h.item()) != 0 for h in host_out):
+    if any(int(h.item()) != 0 for h in host_out):
         raise RuntimeError("e2e: a step flagged non-finite gradients on finite synthetic inputs")
-    h2d_ms = timed(lambda: dev_in[0].copy_(host_in, non_blocking=True))
-    out_bytes = dev_out[0].numel() * dev_out[0].element_size()
-    d2h_ms = timed(lambda: host_out[0].copy_(dev_out[0], non_blocking=True))
-    return e2e_ms, 2 * N * n / (h2d_ms * 1e-3) / 1e9, out_bytes / (d2h_ms * 1e-3) / 1e9
+    cur = torch.cuda.current_stream(device)
+    h2d_ms = timed_block(lambda: dev_in[1].copy_(host_in, non_blocking=True), 3, cur)
+    del dev_in
+    return e2e_ms, nbytes / (h2d_ms * 1e-3) / 1e9, nbytes
+
+
+def unit_step_fn(u, stream, t_counter, copies=("unshard",)):
+    """One step of the unit: the fused kernel on every stepped shard, then the copies."""
+    import fsdp_sharded_mixed_ss_gb300 as ss
+
+    w = u["w"]
+    args = [(k, *u["shard_args"](k)) for k in u["stepped"]]
+
+    def adam():
+        t = t_counter[0]
+        t_counter[0] += 1
+        hp = w.hp(t)
+        for k, n, st, views in args:
+            ss.ss_adam_step(hp, n, *st, rank_grads=views, param16=u["shards"][k], stream=stream)
+
+    def unshard():
+        ss.ss_unshard(u["shards"], u["bounds"], u["flat"], stream=stream)
+
+    def reshard():
+        ss.ss_reshard(u["flat"], u["bounds"], u["shards"], stream=stream)
+
+    fns = {"adam": adam, "unshard": unshard, "reshard": reshard}
+
+    def step():
+        adam()
+        for c in copies:
+            fns[c]()
+
+    return step, fns
+
+
+def time_unit(u, args, stream, peak, copies=("unshard",)):
+    """Step loop, then each kernel of the step alone (back to back, as many launches)."""
+    t_counter = [1]
+    step, fns = unit_step_fn(u, stream, t_counter, copies)
+    ms = run_step_loop(step, args.steps, args.warmup, stream)
+    nb = step_bytes(u)
+    parts = {"adam": (timed_block(fns["adam"], args.steps, stream), nb["adam"], len(u["stepped"]))}
+    for c in copies:
+        parts[c] = (timed_block(fns[c], args.steps, stream), nb["copy"], 1)
+    total = nb["adam"] + nb["copy"] * len(copies)
+    return ms, total, kernel_split(parts, ms, peak)
+
+
+def secondary_blocks(args, device, stream, peak) -> dict:
+    """The GPT-2 small rank-0 shard step + unshard, and the Llama-70B layer: all 64 fp16 shards
+    stepped (one launch each) + unshard + reshard of the flat layer buffer."""
+    import torch
+
+    from synth import workloads
+
+    out = {}
+    for key, w, stepped, copies, steps in (
+            ("gpt2_small_rank0_shard_N8", workloads.gpt2_small(), [0], ("unshard",), max(args.steps, 50)),
+            ("llama70b_layer_N64_fp16_all_shards", workloads.llama70b_layer(), list(range(64)),
+             ("unshard", "reshard"), max(min(args.steps, 10), 3))):
+        u = unit_setup(w, device, stepped, state_whole_unit=len(stepped) > 1)
+        a = argparse.Namespace(steps=steps, warmup=max(args.warmup, 3))
+        ms, total, split = time_unit(u, a, stream, peak, copies)
+        n = sum(u["bounds"][k + 1] - u["bounds"][k] for k in stepped)
+        out[key] = {"workload": w.name, "unit_params": u["P"], "virtual_ranks": u["N"], "stepped_elems": n,
+                    "steps": steps, "ms_per_step": round(ms, 5), "bytes_per_step": total,
+                    "GB/s": round(total / (ms * 1e-3) / 1e9, 1), "frac": round(total / (ms * 1e-3) / 1e9 / peak, 4),
+                    "params_per_s": round(n / (ms * 1e-3), 1), "kernels": split}
+        del u
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args, rank: int, world: int, device):
     import torch
     import torch.distributed as dist
 
-    s = setup(device)
-    ss, w = s["ss"], s["w"]
-    stream = torch.cuda.current_stream(device)
-    t_counter = [1]
+    from synth import workloads
 
-    def step(ev=None):
-        t = t_counter[0]
-        t_counter[0] += 1
-        if ev is not None:
-            ev[0].record(stream)
-        ss.ss_adam_step(w.hp(t), s["n"], s["master"], s["m"], s["v"], rank_grads=s["views"],
-                        param16=s["shards"][0], stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        ss.ss_unshard(s["shards"], s["bounds"], s["flat"], stream=stream)
+    w = workloads.llama3_8b_shard()
+    u = unit_setup(w, device, [0])
+    stream = torch.cuda.current_stream(device)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"]
 
     sampler = ClockSampler(device.index if device.index is not None else 0)
     sampler.start()
     time.sleep(0.3)
+    t_counter = [1]
+    step, fns = unit_step_fn(u, stream, t_counter)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(device)
-    # the fused kernel's own duration, from events around its launch on every 8th timed step
-    # (events between launches cost ~1.5% of a step, so they bracket a sample of the steps only)
-    every = 8
-    evs = {i: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for i in range(0, args.steps, every)}
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize(device)
     h0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        step(evs.get(i))
-    end.record(stream)
-    torch.cuda.synchronize(device)
+    elapsed_ms = timed_block(step, args.steps, stream) * args.steps
     h1 = time.time()
     if world > 1:
         dist.barrier()
-    elapsed_ms = start.elapsed_time(end)
-    adam_ms = statistics.mean(a.elapsed_time(b) for a, b in evs.values())
-    time.sleep(0.25)
+    # each kernel of the step alone, back to back, as many launches as timed steps
+    adam_ms = timed_block(fns["adam"], args.steps, stream)
+    copy_ms = timed_block(fns["unshard"], args.steps, stream)
+    time.sleep(0.2)
     sampler.stop()
     clocks = sampler.summary(h0, h1)
 
-    # end to end through the public API with host buffers: pinned grads in, the step's result out
-    # (its non-finite flag); and, for context, the same with the whole flat unit read back
-    e2e_ms, h2d_gbs, _ = run_e2e(s, args.e2e_steps, device, t_counter, "flag")
-    e2e_p_ms, _, d2h_gbs = run_e2e(s, args.e2e_steps, device, t_counter, "params")
-
-    adam_b, unshard_b = bytes_per_step(s)
-    elapsed_ms, e2e_ms, e2e_p_ms = max_over_ranks([elapsed_ms, e2e_ms, e2e_p_ms], device if world > 1 else None)
+    nb = step_bytes(u)
+    n = u["bounds"][1]
+    elapsed_ms, adam_ms, copy_ms = max_over_ranks([elapsed_ms, adam_ms, copy_ms], device if world > 1 else None)
     ms_per_step = elapsed_ms / args.steps
-    total_bytes = (adam_b + unshard_b) * world
-    value = job_gbs(adam_b + unshard_b, world, ms_per_step)
-    peaks = measured_peaks()
-    achieved = adam_b / (adam_ms * 1e-3) / 1e9
-    traffic = profile_traffic("adam_pipe_kernel")
+    per_step = nb["adam"] + nb["copy"]
+    split = kernel_split({"adam_pipe_kernel": (adam_ms, nb["adam"], 1),
+                          "copy_segments_kernel": (copy_ms, nb["copy"], 1)}, ms_per_step, peak)
+    chk = split["sum_check"]
+    print(f"bench: per-kernel times {adam_ms:.4f} + {copy_ms:.4f} = {chk['sum_ms']:.4f} ms against the step's "
+          f"{ms_per_step:.4f} ms (ratio {chk['ratio']:.4f}, {'within' if chk['within_5pct'] else 'NOT within'} 5%)",
+          file=sys.stderr, flush=True)
+    value = job_gbs(per_step, world, ms_per_step)
+    achieved = nb["adam"] / (adam_ms * 1e-3) / 1e9
+    copy_gbs = nb["copy"] / (copy_ms * 1e-3) / 1e9
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "unit_params": s["P"], "virtual_ranks": s["N"], "shard_elems": s["n"],
+        "config": {"workload": WORKLOAD, "unit_params": u["P"], "virtual_ranks": u["N"], "shard_elems": n,
                    "grad_dtype": "bf16", "param_dtype": "bf16", "state_dtype": "f32",
-                   "bytes_per_step": adam_b + unshard_b,
-                   "l2": "inputs larger than L2 (1.15 GB moved per step vs 129 MB L2); no flush"},
-        "params_per_s": round(s["n"] * world / (ms_per_step * 1e-3), 1),
-        "unit_params_per_s": round(s["P"] * world / (ms_per_step * 1e-3), 1),
-        "roofline": {"kernel": "adam_pipe_kernel (fused reduce + AdamW + bf16 cast, N=8)", "bound": "hbm",
-                     "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": traffic,
-                     "algorithmic_bytes": adam_b, "avg_launch_ms": round(adam_ms, 5),
+                   "grads": "N(0,1e-4) (Irwin-Hall approximation), 1% of entries x100; master N(0,0.02); m=v=0",
+                   "bytes_per_step": per_step, "adam_bytes_per_step": nb["adam"], "unshard_bytes_per_step": nb["copy"],
+                   "l2": f"inputs larger than L2 ({per_step / 1e9:.1f} GB moved per step vs 129 MB L2); no flush"},
+        "params_per_s": round(n * world / (ms_per_step * 1e-3), 1),
+        "unit_params_per_s": round(u["P"] * world / (ms_per_step * 1e-3), 1),
+        "roofline": {"kernel": "adam_pipe_kernel (fused reduce of 8 bf16 ranks + AdamW + bf16 cast)", "bound": "hbm",
+                     "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profile_traffic("adam_pipe_kernel", n),
+                     "algorithmic_bytes": nb["adam"], "avg_launch_ms": round(adam_ms, 5),
+                     "timing": f"{args.steps} back-to-back launches between CUDA events on the launching stream",
                      "peak_source": peaks["source"]},
-        "e2e": {"value": round(total_bytes / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": 2 * s["n"] * s["N"],
-                "d2h_bytes_per_step": 4, "h2d_gbs": round(h2d_gbs, 1),
-                "result": "the step's non-finite-gradient flag (int32), read back every step",
-                "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)",
-                "params_readback": {"value": round(total_bytes / (e2e_p_ms * 1e-3) / 1e9, 1),
-                                    "ms_per_step": round(e2e_p_ms, 4), "d2h_bytes_per_step": 2 * s["P"],
-                                    "d2h_gbs": round(d2h_gbs, 1),
-                                    "note": "the whole flat bf16 unit read back every step instead"}},
+        "roofline_unshard": {"kernel": "copy_segments_kernel (unshard of 8 bf16 shards into the flat unit)",
+                             "bound": "hbm", "achieved": round(copy_gbs, 1), "peak": peak, "unit": "GB/s",
+                             "frac": round(copy_gbs / peak, 4), "algorithmic_bytes": nb["copy"],
+                             "avg_launch_ms": round(copy_ms, 5)},
+        "kernels": split,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
     }
+    if not args.no_e2e:
+        # end to end through the public API with host buffers: the step's gradients in from
+        # pinned host memory, the step's result (its non-finite flag) out, every step
+        e2e_ms, h2d_gbs, in_bytes = run_e2e(u, args.e2e_steps, device, t_counter)
+        e2e_ms = max_over_ranks([e2e_ms], device if world > 1 else None)[0]
+        result["e2e"] = {"value": round(per_step * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                         "ms_per_step": round(e2e_ms, 4), "steps": args.e2e_steps, "h2d_bytes_per_step": in_bytes,
+                         "d2h_bytes_per_step": 4, "h2d_gbs": round(h2d_gbs, 1),
+                         "result": "the step's non-finite-gradient flag (int32), read back every step",
+                         "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)"}
+    del u, fns, step
+    torch.cuda.empty_cache()
+    if not args.no_secondary:
+        result["secondary"] = secondary_blocks(args, device, stream, peak)
     return result
 
 
@@ -467,7 +582,8 @@ def run_suite(args, device) -> dict:
     extra8 = ("adam_step_N8_grads_off_by_one", "grad_reduce_accumulate_N8", "adam_step_N8_fp16_unscale_flag_skip",
               "adam_step_N8_param16_into_flat")
     for N in (2, 8, 64):
-        if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", *(extra8 if N == 8 else ())):
+        off = f"adam_step_N{N}_grads_off_by_one"
+        if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", off, *(extra8 if N == 8 else ())):
             continue
         G = []
         for r in range(N):
@@ -481,12 +597,12 @@ def run_suite(args, device) -> dict:
             out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
         if want(f"grad_sumsq_N{N}"):
             out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
-        if N == 8 and want(extra8[0]):
+        if want(off):
             # gradient views one element off the state's 16-byte phase: the shifted-load kernels
             Gm = [g[1:] for g in G]
             m1 = n - 1
-            out[extra8[0]] = entry(
-                timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1]), 5),
+            out[off] = entry(
+                timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1])),
                 (2 * N + 26) * m1)
         if N == 8 and want(extra8[1]):
             # next rows: gradient accumulation (read-modify-write of the fp32 gradient) ...
@@ -592,15 +708,16 @@ def run_config_steps(ss, device, timed, entry, want=lambda *names: True) -> dict
 # ----------------------------------------------------------------------------- CPU oracle
 
 def oracle_sample_step(sample: int, reps: int):
-    """Time the oracle's shard step (rank-ordered reduce + AdamW + cast, then the unshard copy)
-    on the first `sample` elements of rank 0's shard and the matching slice of every shard."""
+    """Time the oracle's step on the headline workload's inputs: the rank-ordered reduce of the 8
+    ranks' bf16 gradients + AdamW + bf16 cast on the first `sample` elements of rank 0's shard,
+    then the unshard copy of the matching `sample`-element slice of each of the 8 shards."""
     import numpy as np
 
     import oracle
     import synth
     from synth import workloads
 
-    w = workloads.gpt2_small()
+    w = workloads.llama3_8b_shard()
     N = w.n_ranks
     _, bounds = oracle.flatten_layout(w.numels, N)
     grads = [synth.host_range(w.grad(r, 1), 0, sample) for r in range(N)]
@@ -630,9 +747,9 @@ def cpu_baseline(target_s: float = 12.0) -> dict:
     b, times, cores = oracle_sample_step(sample, reps)
     gbs = b * len(times) / sum(times) / 1e9
     return {"value": round(gbs, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{sample} elements of rank 0's shard (8 ranks' bf16 grads) + the matching {sample}-element "
-                      f"slice of each of the 8 shards for the unshard copy; {len(times)} steps, "
-                      f"{sum(times):.1f} s of CPU time"}
+            "sample": f"{sample} elements of the Llama-3-8B rank-0 shard (8 ranks' bf16 grads with outliers) + the "
+                      f"matching {sample}-element slice of each of the 8 shards for the unshard copy; "
+                      f"{len(times)} steps, {sum(times):.1f} s of CPU time"}
 
 
 def run_reference(args):
@@ -645,10 +762,11 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 3), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "unit_params": 124439808, "virtual_ranks": 8, "shard_elems": 15554976,
-                   "sample_elems": sample},
+        "config": {"workload": WORKLOAD, "unit_params": 8_030_261_248, "virtual_ranks": 8,
+                   "shard_elems": 1_003_782_656, "sample_elems": sample},
         "cpu_baseline": {"value": round(gbs, 3), "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": f"{sample} elements of rank 0's shard + matching unshard slices per step"},
+                         "sample": f"{sample} elements of the Llama-3-8B rank-0 shard + the matching slices of the "
+                                   f"8 shards for the unshard, per step"},
         "e2e": {"value": round(gbs, 3), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 

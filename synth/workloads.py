@@ -8,6 +8,12 @@ flattening wrapper concatenates them in. Every input tensor is a seeded
 Streams: gradient of virtual rank r at optimizer step t is
 ``normal(..., kind=GRAD, rank=r, step=t)``; master/m/v use step 0 and are
 indexed by the element's position in the unit's flat parameter vector.
+
+Distributions: every "N(0, s)" below is the generator's Irwin-Hall
+approximation of a normal (the centred sum of twelve uniforms, scaled to
+variance s^2, so its support ends at +-6s), truncated toward zero onto the
+target format's grid; "|N(0, s)|" is its absolute value and "U(-a, a)" one
+53-bit uniform draw, truncated likewise.
 """
 from __future__ import annotations
 
@@ -104,11 +110,15 @@ def gpt2_small(seed: int = 0) -> Workload:
 
 
 def llama3_8b_shard(seed: int = 0) -> Workload:
-    """Llama-3-8B, N=8, one 1/8 shard (rank 0): bf16 grads N(0,1e-4) with 1% of entries x100."""
+    """Llama-3-8B, N=8, one 1/8 shard (rank 0): bf16 grads N(0,1e-4) with 1% of entries x100.
+
+    The other seven shards' bf16 parameters (for the unshard into the flat unit) are seeded
+    N(0, 0.02) streams of their own."""
     return Workload("llama3-8b-shard0-N8", llama3_8b_numels(), 8, BF16,
                     grad=lambda r, t: normal(1e-4, BF16, GRAD, r, t, seed, outlier_every=100, outlier_mult=100.0),
                     master=normal(0.02, FP32, MASTER, seed=seed), m=None, v=None,
-                    steps=1, shards=[0], per_rank_full=False)
+                    steps=1, shards=[0], per_rank_full=False,
+                    param16=lambda k: normal(0.02, BF16, PARAM16, k, 0, seed))
 
 
 def llama70b_layer(seed: int = 0) -> Workload:
