@@ -278,7 +278,9 @@ def ss_grad_sumsq(n: int, sumsq_out, workspace, *, g32=None, rank_grads=None, gd
                                   _stream(stream, sumsq_out)), "ss_grad_sumsq")
 
 
-SS_NOALLOC_SUMSQ_MAX_N = (65536 - 2) * 16384
+# the fixed scratch of ss_grad_sumsq_noalloc (include/ss.h): one fp64 slot per 16,384-element tile, plus two
+SS_NOALLOC_SUMSQ_SLOTS = 65536
+SS_NOALLOC_SUMSQ_MAX_N = (SS_NOALLOC_SUMSQ_SLOTS - 2) * 16384
 
 
 def ss_grad_sumsq_noalloc(n: int, sumsq_out, *, g32=None, rank_grads=None, gdtype: int | None = None,

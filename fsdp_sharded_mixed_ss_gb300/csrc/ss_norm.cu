@@ -2,6 +2,8 @@
 // the reduced gradient (ss_grad_sumsq, and ss_grad_sumsq_noalloc with its slots
 // in a fixed device array) and the clip coefficient from all shards' sums
 // (ss_clip_coef).
+#include <cuda.h>
+
 #include "ss_common.cuh"
 
 namespace ss {
@@ -438,25 +440,69 @@ static __device__ __align__(256) double g_noalloc_sumsq_slots[SS_NOALLOC_SUMSQ_S
 
 namespace {
 
-// Device address of the slot array on the current device. The name of the
-// array is only a host-side stand-in; the address comes from the runtime, once
-// per device, with that device current.
+// The driver's context queries, reached through the runtime (the library does
+// not link the driver library itself): the identity of the current context
+// decides whether a cached address of the slot array is still valid.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// A unique id of the calling thread's current context (ids are never reused
+// within a process), or 0 when there is none or the driver cannot say.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr || get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the slot array in the current context. The name of the
+// array is only a host-side stand-in; the address comes from the runtime, with
+// the device current, the first time a context calls (the array lives in the
+// context's copy of the library's device code, so a device reset, which makes
+// a new context, gets a new lookup). Without a context id the lookup runs on
+// every call.
 ss_status noalloc_slots(double** out) {
-  constexpr int kMaxDevices = 64;
+  constexpr int kCached = 64;
   static std::mutex mu;
-  static double* addr[kMaxDevices] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= kMaxDevices) return SS_ERR_INVALID_ARG;
+  static unsigned long long ids[kCached] = {};
+  static double* addrs[kCached] = {};
+  static int next = 0;
   std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_sumsq_slots);
-    if (e != cudaSuccess) return cuda_fail(e);
-    addr[dev] = static_cast<double*>(p);
+  const unsigned long long id = current_context_id();
+  if (id != 0) {
+    for (int i = 0; i < kCached; ++i) {
+      if (ids[i] == id) {
+        *out = addrs[i];
+        return SS_OK;
+      }
+    }
   }
-  *out = addr[dev];
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_sumsq_slots);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // the lookup above makes the device's context current if nothing was, so ask again
+  const unsigned long long now = id != 0 ? id : current_context_id();
+  if (now != 0) {
+    ids[next] = now;
+    addrs[next] = static_cast<double*>(p);
+    next = (next + 1) % kCached;
+  }
+  *out = static_cast<double*>(p);
   return SS_OK;
 }
 

@@ -218,8 +218,11 @@ ss_status ss_clip_coef(const double* shard_sumsq, int32_t n_shards, float max_no
  *   - n may be at most SS_NOALLOC_SUMSQ_MAX_N (1,073,709,056 elements);
  *     larger n returns SS_ERR_OVERFLOW and launches nothing.
  *   - The first call on a device looks up the array's device address with
- *     the runtime (no allocation); make that first call before any stream
- *     capture on that device.
+ *     the runtime (no allocation) and caches it for the device's CUDA
+ *     context; make that first call before any stream capture on that
+ *     device. A device reset (cudaDeviceReset) ends the context and with it
+ *     the array's contents and address: the next call looks the address up
+ *     again, so make it, too, outside a stream capture.
  *   - All calls share the one array: calls whose kernels may overlap on the
  *     GPU (different streams without ordering) race and give wrong results.
  *     Calls ordered on one stream are safe; nothing has to be cleared between

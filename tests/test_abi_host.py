@@ -156,9 +156,38 @@ def test_sumsq_and_clip_argument_errors(ss):
     assert e.value.status == 3
 
 
+def _header_defines():
+    """The integer #defines of include/ss.h, evaluated the way the C preprocessor would for these
+    simple forms (a literal, or an expression over earlier defines and an int64 cast)."""
+    import re
+
+    path = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ss.h")
+    env = {}
+    with open(path) as f:
+        for line in f:
+            m = re.match(r"#define\s+(SS_\w+)\s+(.+)$", line.strip())
+            if not m:
+                continue
+            expr = m.group(2).replace("(int64_t)", "")
+            try:
+                env[m.group(1)] = int(eval(expr, {}, dict(env)))
+            except Exception:  # not an integer expression
+                pass
+    return env
+
+
 def test_noalloc_size_limit_rejected_on_host(ss):
     # n above the fixed scratch capacity is refused before anything touches a GPU
     with pytest.raises(ss.SSError) as e:
         ss.ss_grad_sumsq_noalloc(ss.SS_NOALLOC_SUMSQ_MAX_N + 1, 0x70000000, g32=0x71000000, stream=0)
     assert e.value.status == 5
-    assert ss.SS_NOALLOC_SUMSQ_MAX_N == (65536 - 2) * 16384
+
+
+def test_noalloc_limit_follows_the_header_and_the_workspace_rule(ss):
+    """The binding's limit is the header's, and it is exactly the largest shard whose workspace
+    (as the library itself sizes it) fits the fixed slot array."""
+    d = _header_defines()
+    slots, max_n = d["SS_NOALLOC_SUMSQ_SLOTS"], d["SS_NOALLOC_SUMSQ_MAX_N"]
+    assert ss.SS_NOALLOC_SUMSQ_MAX_N == max_n
+    assert ss.ss_grad_sumsq_workspace(max_n) <= 8 * slots
+    assert ss.ss_grad_sumsq_workspace(max_n + 1) > 8 * slots
