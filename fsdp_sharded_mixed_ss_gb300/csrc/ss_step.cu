@@ -414,8 +414,8 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
 // 31 the chunk under the start of the group after the run) and sums the
 // ranks' chunks element by element in rank order -- the same fp32 sum each
 // element gets anywhere else, only held in a neighbouring register -- then
-// lanes 0..30 take the upper lane's 8 sums with shuffles and pick their
-// group's 8 out of the 16. Each gradient byte is loaded once; lanes 0..30
+// each lane moves its group's sums into place, taking the ones past its own
+// chunk from the upper lane by shuffle. Each gradient byte is loaded once; lanes 0..30
 // load their group's state; the loads of the warp's next run are issued
 // before the current run's update, as in the aligned double-buffered kernel.
 // Every chunk lies under a group in [1, nvec - 1], so inside its array; the
@@ -446,11 +446,19 @@ __device__ __forceinline__ void shift_pipe_load(const ShiftArgs<MAXR>& x, int64_
   }
 }
 
-// g[i] = element SH + i of the 16 values (c, d).
+// c <- elements SH .. SH + 7 of the 16 values (this lane's c, the next lane's c),
+// in place: only the SH values that come from the next lane are shuffled, and
+// they are taken before c is moved down (all lanes of the warp call it with
+// the same SH).
 template <int SH>
-__device__ __forceinline__ void take8(const float (&c)[8], const float (&d)[8], float (&g)[8]) {
+__device__ __forceinline__ void shift_down8(float (&c)[8]) {
+  float d[SH > 0 ? SH : 1];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) g[i] = SH + i < 8 ? c[SH + i] : d[SH + i - 8];
+  for (int j = 0; j < SH; ++j) d[j] = __shfl_down_sync(0xFFFFFFFFu, c[j], 1);
+#pragma unroll
+  for (int i = 0; i + SH < 8; ++i) c[i] = c[i + SH];
+#pragma unroll
+  for (int j = 0; j < SH; ++j) c[8 - SH + j] = d[j];
 }
 
 template <int GT, int PT, bool WRITE_P16, int MAXR, int NR>
@@ -472,21 +480,19 @@ __global__ void __launch_bounds__(kThreads, 2) adam_shift_pipe_kernel(const __gr
   if (warp < runs) shift_pipe_load<GT, NR>(x, warp, lane, nvec, cur);
   for (int64_t run = warp; run < runs; run += nwarps) {  // warp-uniform
     if (run + nwarps < runs) shift_pipe_load<GT, NR>(x, run + nwarps, lane, nvec, nxt);
-    float c[8], d[8], g[8];
-    widen8<GT>(cur.r[0], c);
+    float g[8];
+    widen8<GT>(cur.r[0], g);
 #pragma unroll
-    for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], c);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = __shfl_down_sync(0xFFFFFFFFu, c[i], 1);
-    switch (sh) {
-      case 0: take8<0>(c, d, g); break;
-      case 1: take8<1>(c, d, g); break;
-      case 2: take8<2>(c, d, g); break;
-      case 3: take8<3>(c, d, g); break;
-      case 4: take8<4>(c, d, g); break;
-      case 5: take8<5>(c, d, g); break;
-      case 6: take8<6>(c, d, g); break;
-      default: take8<7>(c, d, g); break;
+    for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
+    switch (sh) {  // warp-uniform
+      case 0: break;
+      case 1: shift_down8<1>(g); break;
+      case 2: shift_down8<2>(g); break;
+      case 3: shift_down8<3>(g); break;
+      case 4: shift_down8<4>(g); break;
+      case 5: shift_down8<5>(g); break;
+      case 6: shift_down8<6>(g); break;
+      default: shift_down8<7>(g); break;
     }
     const int64_t gi = 1 + run * kRun + lane;
     if (lane < kRun && gi < nvec - 1) {
