@@ -322,7 +322,13 @@ def run_e2e(u, steps: int, device, t_counter):
               torch.empty((N, n), dtype=src.dtype, device=device)]
     flags = [torch.zeros(1, dtype=torch.int32, device=device) for _ in range(2)]
     host_out = [torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
-    s_h2d, s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(3))
+    s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(2))
+    # the gradients go in as 256 MB pieces spread over four copy streams: on the GB300 machine one
+    # stream of back-to-back pieces moved ~105 GB/s, four streams (or one 16 GB copy) ~210 GB/s
+    s_h2d = [torch.cuda.Stream(device) for _ in range(4)]
+    piece = 256 << 20
+    src_b = host_in.view(torch.uint8).view(-1)
+    dst_b = [d.view(torch.uint8).view(-1) for d in dev_in]
     done = {"h2d": {}, "cmp": {}, "d2h": {}}
     n0, st, _ = u["shard_args"](0)
 
@@ -331,16 +337,27 @@ def run_e2e(u, steps: int, device, t_counter):
         e.record(s)
         done[kind][i] = e
 
+    def copy_in(j, after=None):
+        evs = []
+        for q, s in enumerate(s_h2d):
+            if after is not None:
+                s.wait_event(after)
+            with torch.cuda.stream(s):
+                for o in range(q * piece, nbytes, len(s_h2d) * piece):
+                    dst_b[j][o:o + piece].copy_(src_b[o:o + piece], non_blocking=True)
+            e = torch.cuda.Event()
+            e.record(s)
+            evs.append(e)
+        return evs
+
     def step(i):
         j = i % 2
         t = t_counter[0]
         t_counter[0] += 1
-        if i - 2 in done["cmp"]:
-            s_h2d.wait_event(done["cmp"][i - 2])          # dev_in[j] no longer read
-        with torch.cuda.stream(s_h2d):
-            dev_in[j].copy_(host_in, non_blocking=True)
-        mark("h2d", i, s_h2d)
-        s_cmp.wait_event(done["h2d"][i])
+        evs = copy_in(j, done["cmp"].get(i - 2))          # dev_in[j] no longer read by step i - 2
+        done["h2d"][i] = evs[-1]
+        for e in evs:
+            s_cmp.wait_event(e)
         if i - 2 in done["d2h"]:
             s_cmp.wait_event(done["d2h"][i - 2])          # flags[j] already copied out
         with torch.cuda.stream(s_cmp):
@@ -360,10 +377,13 @@ def run_e2e(u, steps: int, device, t_counter):
     for d in done.values():
         d.clear()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(s_h2d)
+    e0.record(s_h2d[0])
+    for s in s_h2d[1:]:
+        s.wait_event(e0)
     for i in range(steps):
         step(i)
-    s_d2h.wait_stream(s_h2d)
+    for s in s_h2d:
+        s_d2h.wait_stream(s)
     s_d2h.wait_stream(s_cmp)
     e1.record(s_d2h)
     torch.cuda.synchronize(device)
@@ -371,7 +391,15 @@ def run_e2e(u, steps: int, device, t_counter):
     if any(int(h.item()) != 0 for h in host_out):
         raise RuntimeError("e2e: a step flagged non-finite gradients on finite synthetic inputs")
     cur = torch.cuda.current_stream(device)
-    h2d_ms = timed_block(lambda: dev_in[1].copy_(host_in, non_blocking=True), 3, cur)
+
+    def copy_alone():
+        a = torch.cuda.Event()
+        a.record(cur)
+        for e in copy_in(1, a):
+            cur.wait_event(e)
+
+    copy_alone()
+    h2d_ms = timed_block(copy_alone, 3, cur)
     del dev_in
     return e2e_ms, nbytes / (h2d_ms * 1e-3) / 1e9, nbytes
 
@@ -526,7 +554,8 @@ def run_ours(args, rank: int, world: int, device):
                          "ms_per_step": round(e2e_ms, 4), "steps": args.e2e_steps, "h2d_bytes_per_step": in_bytes,
                          "d2h_bytes_per_step": 4, "h2d_gbs": round(h2d_gbs, 1),
                          "result": "the step's non-finite-gradient flag (int32), read back every step",
-                         "pipeline": "h2d of step i+1 and d2h of step i-1 overlap step i (3 streams, double buffers)"}
+                         "pipeline": "h2d of step i+1 (256 MB pieces over 4 copy streams) and d2h of step i-1 "
+                                     "overlap step i (double-buffered device gradients)"}
     del u, fns, step
     torch.cuda.empty_cache()
     if not args.no_secondary:
@@ -624,6 +653,22 @@ def run_suite(args, device) -> dict:
             del flat
         del G
         torch.cuda.empty_cache()
+    # the fused step with every rank's gradient view one element off the state's phase, across
+    # rank counts (the shifted-load kernel forms)
+    if want("adam_step_off_by_one_by_ranks"):
+        G = []
+        for r in range(32):
+            t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
+            synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+            G.append(t[1:n])
+        m1 = n - 1
+        by_ranks = {}
+        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 32):
+            Gn = G[:N]
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gn,
+                                                                  param16=p16[:m1])), (2 * N + 26) * m1)
+        out["adam_step_off_by_one_by_ranks"] = by_ranks
+        del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):
         G = []

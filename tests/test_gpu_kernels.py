@@ -388,9 +388,9 @@ def test_step_split_calls_agree(ss):
 @pytest.mark.parametrize("same", [True, False])
 def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
     """Rank views off the aligned state's phase: all at one offset (1..7, the warp-cooperative
-    kernel for N <= 8) or rank r at (r % 7) + 1 (mixed phases: the per-thread kernel), from a
-    1-group body (n = 27) to many runs per warp; equal to the aligned kernel bit for bit and to
-    the oracle."""
+    kernels: double-buffered for N <= 8, single-buffered for 9) or rank r at (r % 7) + 1 (mixed
+    phases: the per-thread kernel), from a 1-group body (n = 27) to many runs per warp; equal to
+    the aligned kernel bit for bit and to the oracle."""
     import torch
     hp = dict(HP, step=5)
     ref = _oracle_step(n, N, fmt, hp)
@@ -406,6 +406,33 @@ def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
         assert torch.equal(x, y)
     assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
     _check(*b, pb, ref, fmt)
+
+
+@pytest.mark.parametrize("N", [2, 8, 16])
+@pytest.mark.parametrize("warps_per_sm", [12, 16])
+@pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, 7), (3, -5)])
+def test_step_shifted_run_boundaries(ss, N, warps_per_sm, k, d):
+    """The warp-cooperative shifted-load kernels take runs of 31 groups from a per-block counter;
+    their grid passes over k x (SMs x resident warps) runs (12 or 16 warps per SM, by block shape),
+    so shard lengths whose body is just a whole number of passes, or one run more or less, check
+    that every run is taken exactly once (2 and 8 ranks: double-buffered; 16: single-buffered),
+    with the gradient views one element off the state's phase: all of the state against the
+    oracle, and bit-equal to the aligned kernel."""
+    import torch
+    runs = k * _sms() * warps_per_sm + d
+    n = (runs * 31 + 2) * 8 + 3          # body groups 1 .. nvec - 2, plus a 3-element tail
+    ref = _oracle_step(n, N, synth.BF16, HP)
+    G_al = [dev_bits(s, n) for s in ref[0]]
+    G_off = [dev_bits(s, n, offset=1) for s in ref[0]]
+    a, b = _state(n), _state(n)
+    pa = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    pb = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(HP, n, *a, rank_grads=G_al, param16=pa)
+    ss.ss_adam_step(HP, n, *b, rank_grads=G_off, param16=pb)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+    _check(*b, pb, ref, synth.BF16)
 
 
 @pytest.mark.parametrize("goffs,poff", [((1,) * 8, 0), ((0, 1, 2, 3, 4, 5, 6, 7), 3), ((3,) * 8, 1)])
