@@ -614,7 +614,9 @@ def run_suite(args, device) -> dict:
               "adam_step_N8_param16_into_flat")
     for N in (2, 8, 64):
         off = f"adam_step_N{N}_grads_off_by_one"
-        if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", off, *(extra8 if N == 8 else ())):
+        mixed = f"adam_step_N{N}_grads_mixed_phase"
+        if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", off, mixed,
+                    *(extra8 if N == 8 else ())):
             continue
         G = []
         for r in range(N):
@@ -635,6 +637,14 @@ def run_suite(args, device) -> dict:
             out[off] = entry(
                 timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gm, param16=p16[:m1])),
                 (2 * N + 26) * m1)
+        if want(mixed):
+            # rank r's gradient view (r % 7) + 1 elements off the state's phase: every rank shifted by its own
+            # phase (views into one stacked buffer whose row length is not a multiple of 8 look like this)
+            m7 = n - 7
+            Gx = [g[(r % 7) + 1:(r % 7) + 1 + m7] for r, g in enumerate(G)]
+            out[mixed] = entry(
+                timed(lambda: ss.ss_adam_step(hp, m7, *(t[:m7] for t in st), rank_grads=Gx, param16=p16[:m7])),
+                (2 * N + 26) * m7)
         if N == 8 and want(extra8[1]):
             # next rows: gradient accumulation (read-modify-write of the fp32 gradient) ...
             out[extra8[1]] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32, accumulate=True)), (2 * N + 8) * n)
@@ -657,19 +667,23 @@ def run_suite(args, device) -> dict:
         torch.cuda.empty_cache()
     # the fused step with every rank's gradient view one element off the state's phase, across
     # rank counts (the shifted-load kernel forms)
-    if want("adam_step_off_by_one_by_ranks"):
+    # (and with rank r's view (r % 7) + 1 elements off: every rank at its own phase)
+    for key, offset in (("adam_step_off_by_one_by_ranks", lambda r: 1),
+                        ("adam_step_mixed_phase_by_ranks", lambda r: (r % 7) + 1)):
+        if not want(key):
+            continue
+        m7 = n - 7
         G = []
-        for r in range(32):
+        for r in range(64):
             t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
-            G.append(t[1:n])
-        m1 = n - 1
+            G.append(t[offset(r):offset(r) + m7])
         by_ranks = {}
-        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 32):
+        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 32, 64):
             Gn = G[:N]
-            by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, m1, *(t[:m1] for t in st), rank_grads=Gn,
-                                                                  param16=p16[:m1])), (2 * N + 26) * m1)
-        out["adam_step_off_by_one_by_ranks"] = by_ranks
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, m7, *(t[:m7] for t in st), rank_grads=Gn,
+                                                                  param16=p16[:m7])), (2 * N + 26) * m7)
+        out[key] = by_ranks
         del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):

@@ -1,7 +1,7 @@
 """Build step of the shard-step library: compiles csrc/ into libss.so with nvcc for sm_103a.
 
-One translation unit per part of the ABI (host layout code; the fused step;
-the reduce; the norm clip; the copies; shared host helpers), compiled in
+One translation unit per part of the ABI (host layout code; the fused step,
+in two parts by the arrays' alignment; the reduce; the norm clip; the copies; shared host helpers), compiled in
 parallel by nvcc and linked against the shared CUDA runtime so the library
 shares the runtime instance of the process that loads it (e.g. PyTorch's).
 """
@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libss.so")
 
-SOURCES = ["ss_layout.cpp", "ss_util.cu", "ss_step.cu", "ss_reduce.cu", "ss_norm.cu", "ss_copy.cu"]
+SOURCES = ["ss_layout.cpp", "ss_util.cu", "ss_step.cu", "ss_step_shift.cu", "ss_reduce.cu", "ss_norm.cu", "ss_copy.cu"]
 
 
 def nvcc() -> str:

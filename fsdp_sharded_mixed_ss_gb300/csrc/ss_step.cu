@@ -1,38 +1,15 @@
 // ss_step.cu -- the fused shard step (ss_adam_step): rank-ordered fp32 reduce of
 // the ranks' gradient shards, AdamW on the fp32 master and moments, and the
-// 16-bit parameter cast, in one pass over HBM. Six kernel forms share the
-// per-element arithmetic of ss_math.cuh: register double-buffered (up to 8
-// ranks or an fp32 gradient), single-buffered vector (more ranks), three with
-// shifted loads for 16-bit arrays off the state's 16-byte phase (for ranks at
-// one phase a warp-cooperative double-buffered one up to 8 ranks and a
-// warp-cooperative single-buffered one above; a per-thread one for ranks at
-// mixed phases) and element-wise.
-#include "ss_common.cuh"
+// 16-bit parameter cast, in one pass over HBM. This file holds the entry point
+// and the kernel forms for arrays that share the fp32 state's 16-byte phase:
+// register double-buffered (up to 8 ranks or an fp32 gradient),
+// single-buffered vector (more ranks) and element-wise (no common phase). The
+// forms for 16-bit arrays off that phase are in ss_step_shift.cu. All share
+// the per-element arithmetic of ss_math.cuh.
+#include "ss_step.cuh"
 
 namespace ss {
 namespace {
-
-// ------------------------------------------------------------------ fused AdamW step
-
-template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
-__device__ __forceinline__ void step1(const StepArgs<MAXR>& a, int64_t e, float gs, bool& bad) {
-  float g;
-  if constexpr (FROM_G32) {
-    g = a.g32[e];
-  } else {
-    g = reduce1<GT>(a.ranks, a.n_ranks, e);
-    if (a.post_scale != 1.0f) g = g * a.post_scale;
-  }
-  bad |= !finite(g);
-  if (a.g_out) a.g_out[e] = g;
-  if (a.dev_scale) g = g * gs;
-  float p = a.master[e], m = a.m[e], v = a.v[e];
-  adamw_elem(a.k, g, p, m, v);
-  a.master[e] = p;
-  a.m[e] = m;
-  a.v[e] = v;
-  if constexpr (WRITE_P16) static_cast<uint16_t*>(a.p16)[e] = narrow1<PT>(p);
-}
 
 // Rank counts up to which the single-buffered kernel also prefetches its
 // warp's next groups into L2 (measured on GB300 at 2^26 elements: +3-12% for
@@ -283,436 +260,6 @@ __global__ void __launch_bounds__(kThreads) adam_scalar_kernel(const __grid_cons
   }
 }
 
-// ------------------------------------------------------------------ fused AdamW step, 16-bit arrays off the state's phase
-//
-// When the fp32 arrays share a 16-byte phase but some 16-bit arrays (rank
-// gradients, param16) do not -- shard views at boundaries that are not
-// multiples of 8 elements, or param16 inside a flat buffer at such a
-// boundary -- groups still start where the fp32 arrays are 16-byte aligned.
-// Every 16-bit gradient array is read as the two aligned 16-byte chunks that
-// hold the group (all loads issued first) and funnel-shifted to its phase;
-// param16 is stored in 4- or 2-byte pieces when it is off phase. The body is
-// groups 1 .. nvec-2, so every chunk read lies inside its array; the first
-// and last groups and the head/tail elements are done one by one.
-template <int MAXR>
-struct ShiftArgs {
-  StepArgs<MAXR> s;
-  uint8_t rphase[MAXR];  // byte offset of each rank's group starts past a 16-byte boundary (even)
-  uint8_t pphase;        // the same for param16
-};
-
-// The 16 bytes that start `phase` bytes into the 32-byte window (a, b).
-__device__ __forceinline__ uint4 window_at(const uint4& a, const uint4& b, int phase) {
-  switch (phase) {
-    case 0: return a;
-    case 2: return window16<2>(a, b);
-    case 4: return window16<4>(a, b);
-    case 6: return window16<6>(a, b);
-    case 8: return window16<8>(a, b);
-    case 10: return window16<10>(a, b);
-    case 12: return window16<12>(a, b);
-    default: return window16<14>(a, b);
-  }
-}
-
-__device__ __forceinline__ void st16_at_phase(void* p, const uint4& v, int phase) {
-  if (phase == 0) {
-    __stcs(reinterpret_cast<uint4*>(p), v);
-  } else if ((phase & 3) == 0) {
-    uint32_t* q = static_cast<uint32_t*>(p);
-    q[0] = v.x; q[1] = v.y; q[2] = v.z; q[3] = v.w;
-  } else {
-    uint16_t* q = static_cast<uint16_t*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      q[2 * i] = static_cast<uint16_t>(w[i] & 0xFFFFu);
-      q[2 * i + 1] = static_cast<uint16_t>(w[i] >> 16);
-    }
-  }
-}
-
-template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
-__global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
-  pdl_wait();
-  pdl_trigger();
-  const StepArgs<MAXR>& a = x.s;
-  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
-  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
-  const int64_t nvec = (a.n - a.head) / kGroup;
-  const int64_t g_lo = nvec >= 3 ? 1 : 0, g_hi = nvec >= 3 ? nvec - 1 : 0;  // vector body [g_lo, g_hi)
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  bool bad = false;
-  for (int64_t gi = g_lo + tid; gi < g_hi; gi += stride) {
-    const int64_t e = a.head + gi * kGroup;
-    float g[8];
-    if constexpr (FROM_G32) {
-      ld8f(a.g32 + e, g);
-    } else {
-      for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
-        // both aligned chunks around every rank's group, all loads issued before any use
-        // (in the body the second chunk is always inside the array, even at phase 0)
-        uint4 c0[8], c1[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (r0 + j < a.n_ranks) {
-            const uint4* c = reinterpret_cast<const uint4*>(
-                reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + e) - x.rphase[r0 + j]);
-            c0[j] = __ldcs(c);
-            c1[j] = __ldcs(c + 1);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (r0 + j < a.n_ranks) {
-            const uint4 w = window_at(c0[j], c1[j], x.rphase[r0 + j]);
-            if (r0 + j == 0) widen8<GT>(w, g);
-            else add8<GT>(w, g);
-          }
-        }
-      }
-      if (a.post_scale != 1.0f) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
-      }
-    }
-    if (a.nonfinite) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-    }
-    if (a.g_out) st8f(a.g_out + e, g);
-    if (a.dev_scale) {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
-    }
-    float p[8], m[8], v[8];
-    ld8f(a.master + e, p);
-    ld8f(a.m + e, m);
-    ld8f(a.v + e, v);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
-    st8f(a.master + e, p);
-    st8f(a.m + e, m);
-    st8f(a.v + e, v);
-    if constexpr (WRITE_P16) st16_at_phase(static_cast<uint16_t*>(a.p16) + e, narrow8<PT>(p), x.pphase);
-  }
-  // everything outside the vector body, one element per thread (< 31 elements)
-  const int64_t lo_end = a.head + g_lo * kGroup, hi_start = a.head + g_hi * kGroup;
-  const int64_t n_edge = lo_end + (a.n - hi_start);
-  if (tid < n_edge) step1<GT, PT, FROM_G32, WRITE_P16>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), gs, bad);
-  if (a.nonfinite) {
-    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
-    if (any && (threadIdx.x & 31) == 0) *a.nonfinite = 1;
-  }
-}
-
-// Warp-cooperative forms of the shifted-load step for 16-bit rank gradients
-// that all sit at the same 16-byte phase (views at one offset into
-// identically allocated buffers, the usual case). A warp takes runs of 31
-// consecutive groups of the vector body: lane j loads, per rank, the aligned
-// 16-byte chunk under the start of group j of the run (lane 31 the chunk under
-// the start of the group after the run) and sums the ranks' chunks element by
-// element in rank order -- the same fp32 sum each element gets anywhere else,
-// only held in a neighbouring register -- then each lane moves its group's
-// sums into place, taking the ones past its own chunk from the upper lane by
-// shuffle. Each gradient byte is loaded once; lanes 0..30 load and update
-// their group's state. Every chunk lies under a group in [1, nvec - 1], so
-// inside its array; the groups outside the body [1, nvec - 1) and the
-// head/tail elements are done one by one. Runs are taken from a per-block
-// counter in shared memory and owned round robin, as the aligned kernels take
-// their chunks.
-//
-// Up to 8 ranks: register double-buffered (the loads of the warp's next run
-// are issued before the current run's update). The double-float update and
-// two runs' loads need more than 128 registers from 4 ranks on, so the block
-// shape depends on the rank count: up to 3 ranks one 512-thread block per SM
-// (128 registers) with an L2 prefetch of the run after next, from 4 ranks one
-// 384-thread block per SM (up to 170 registers) without it. Measured on GB300
-// at 2^26 elements with the gradients one element off phase: 8 ranks 0.82 of
-// the copy peak in the 128-register form (it spilled), 0.96 in this one;
-// 1-8 ranks 0.92-1.01. The prefetch gained 1-3% at 2-3 ranks and cost 3-6%
-// at 4-6.
-// More ranks: single-buffered, each run's state requested with the first
-// batch of 8 rank chunks, all loads of a batch before its adds (16 and 32
-// ranks 0.99 of the copy peak; 9-12 ranks only 0.77-0.82 -- one batch of 8
-// and a short second one, where the update's issue time is no longer hidden
-// behind memory).
-constexpr int kRun = 31;  // groups per warp run
-
-#ifndef SS_SHIFT_NARROW_RANKS
-#define SS_SHIFT_NARROW_RANKS 3  // up to this many ranks: one 512-thread block per SM (128 registers)
-#endif
-#ifndef SS_SHIFT_WIDE_THREADS
-#define SS_SHIFT_WIDE_THREADS 384  // above: one 384-thread block per SM (up to 170 registers)
-#endif
-#ifndef SS_SHIFT_WIDE_BLOCKS
-#define SS_SHIFT_WIDE_BLOCKS 1
-#endif
-// Rank counts up to which the warp-cooperative kernels also prefetch a later
-// run's bytes into L2 (as the aligned kernels do for few ranks).
-#ifndef SS_SHIFT_PF_RANKS
-#define SS_SHIFT_PF_RANKS 3
-#endif
-#ifndef SS_SHIFT_VEC_PF_RANKS
-#define SS_SHIFT_VEC_PF_RANKS 13
-#endif
-template <int NR>
-struct ShiftShape {
-  static constexpr bool kNarrow = NR <= SS_SHIFT_NARROW_RANKS;
-  static constexpr int kThreadsPerBlock = kNarrow ? kChunkThreads : SS_SHIFT_WIDE_THREADS;
-  static constexpr int kBlocksPerSm = kNarrow ? kChunkBlocksPerSm : SS_SHIFT_WIDE_BLOCKS;
-};
-
-template <int GT, int NR, int MAXR>
-__device__ __forceinline__ void shift_pipe_load(const ShiftArgs<MAXR>& x, int64_t run, int lane, int64_t nvec,
-                                                PipeGroup<NR>& G) {
-  const StepArgs<MAXR>& a = x.s;
-  int64_t gi = 1 + run * kRun + lane;  // the group whose start this lane's chunks cover
-  gi = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the array, unused
-  const int64_t e = a.head + gi * kGroup;
-#pragma unroll
-  for (int r = 0; r < NR; ++r)
-    G.r[r] = __ldcs(reinterpret_cast<const uint4*>(
-        reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e) - x.rphase[0]));
-  if (lane < kRun) {
-    const int64_t gb = gi < nvec - 2 ? gi : nvec - 2;  // the state of a body group
-    const int64_t es = a.head + gb * kGroup;
-    G.s[0] = __ldcs(reinterpret_cast<const float4*>(a.master + es));
-    G.s[1] = __ldcs(reinterpret_cast<const float4*>(a.master + es) + 1);
-    G.s[2] = __ldcs(reinterpret_cast<const float4*>(a.m + es));
-    G.s[3] = __ldcs(reinterpret_cast<const float4*>(a.m + es) + 1);
-    G.s[4] = __ldcs(reinterpret_cast<const float4*>(a.v + es));
-    G.s[5] = __ldcs(reinterpret_cast<const float4*>(a.v + es) + 1);
-  }
-}
-
-// L2 prefetch of run `run`'s bytes, one bulk prefetch per array (lane r < n_ranks
-// takes rank r's gradient chunks, the next three lanes master, m and v): the
-// same chunks and state the run's loads read, so every range lies inside its
-// array, starts on a 16-byte boundary and is a multiple of 16 bytes. Hints only.
-template <int MAXR>
-__device__ __forceinline__ void shift_prefetch(const ShiftArgs<MAXR>& x, int64_t run, int lane, int n_ranks,
-                                               int64_t nvec) {
-  const StepArgs<MAXR>& a = x.s;
-  if (lane >= n_ranks + 3) return;
-  const int64_t g0 = 1 + run * kRun;
-  if (lane < n_ranks) {
-    const int64_t gl = g0 + kRun < nvec - 1 ? g0 + kRun : nvec - 1;  // the chunk after the run, if any
-    prefetch_l2(reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[lane]) + a.head + g0 * kGroup) -
-                    x.rphase[0],
-                static_cast<uint32_t>((gl - g0 + 1) * 16));
-  } else {
-    const int64_t gb = g0 + kRun - 1 < nvec - 2 ? g0 + kRun - 1 : nvec - 2;  // the run's last body group
-    const int k = lane - n_ranks;
-    prefetch_l2((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + a.head + g0 * kGroup,
-                static_cast<uint32_t>((gb - g0 + 1) * 32));
-  }
-}
-
-// c <- elements SH .. SH + 7 of the 16 values (this lane's c, the next lane's c),
-// in place: only the SH values that come from the next lane are shuffled, and
-// they are taken before c is moved down (all lanes of the warp call it with
-// the same SH).
-template <int SH>
-__device__ __forceinline__ void shift_down8(float (&c)[8]) {
-  float d[SH > 0 ? SH : 1];
-#pragma unroll
-  for (int j = 0; j < SH; ++j) d[j] = __shfl_down_sync(0xFFFFFFFFu, c[j], 1);
-#pragma unroll
-  for (int i = 0; i + SH < 8; ++i) c[i] = c[i + SH];
-#pragma unroll
-  for (int j = 0; j < SH; ++j) c[8 - SH + j] = d[j];
-}
-
-__device__ __forceinline__ void shift_down8(float (&g)[8], int sh) {
-  switch (sh) {  // warp-uniform
-    case 0: break;
-    case 1: shift_down8<1>(g); break;
-    case 2: shift_down8<2>(g); break;
-    case 3: shift_down8<3>(g); break;
-    case 4: shift_down8<4>(g); break;
-    case 5: shift_down8<5>(g); break;
-    case 6: shift_down8<6>(g); break;
-    default: shift_down8<7>(g); break;
-  }
-}
-
-// The update of one body group from its (shifted) gradient sums and its state;
-// the options and the param16 store at its phase, as in the aligned kernels.
-template <int PT, bool WRITE_P16, int MAXR>
-__device__ __forceinline__ void shift_update(const ShiftArgs<MAXR>& x, int64_t e, float (&g)[8], float (&p)[8],
-                                             float (&m)[8], float (&v)[8], float gs, bool& bad) {
-  const StepArgs<MAXR>& a = x.s;
-  if (a.post_scale != 1.0f) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
-  }
-  if (a.nonfinite) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-  }
-  if (a.g_out) st8f(a.g_out + e, g);
-  if (a.dev_scale) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
-  st8f(a.master + e, p);
-  st8f(a.m + e, m);
-  st8f(a.v + e, v);
-  if constexpr (WRITE_P16) st16_at_phase(static_cast<uint16_t*>(a.p16) + e, narrow8<PT>(p), x.pphase);
-}
-
-// Everything outside the vector body [1, nvec - 1), one element per thread (< 31 elements).
-template <int GT, int PT, bool WRITE_P16, int MAXR>
-__device__ __forceinline__ void shift_edges(const ShiftArgs<MAXR>& x, int64_t nvec, float gs, bool& bad) {
-  const StepArgs<MAXR>& a = x.s;
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t lo_end = a.head + kGroup, hi_start = a.head + (nvec - 1) * kGroup;
-  const int64_t n_edge = lo_end + (a.n - hi_start);
-  if (tid < n_edge) step1<GT, PT, false, WRITE_P16>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), gs, bad);
-}
-
-template <int GT, int PT, bool WRITE_P16, int MAXR, int NR>
-__global__ void __launch_bounds__(ShiftShape<NR>::kThreadsPerBlock, ShiftShape<NR>::kBlocksPerSm)
-    adam_shift_pipe_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
-  __shared__ unsigned next_run;
-  if (threadIdx.x == 0) next_run = 0;
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  const StepArgs<MAXR>& a = x.s;
-  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
-  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
-  const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
-  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
-  const int sh = x.rphase[0] >> 1;                // the groups' element offset into their first chunk
-  const int lane = threadIdx.x & 31;
-  const ChunkMap<ShiftShape<NR>::kThreadsPerBlock / 32> map(runs * 32);  // one "chunk" per run
-  constexpr bool kPrefetch = NR <= SS_SHIFT_PF_RANKS;
-  bool bad = false;
-  PipeGroup<NR> cur, nxt;
-  // The warp's runs in the order it takes them: `run` (in cur), the next one (loaded into
-  // nxt during run's update) and, with the L2 prefetch, the one after (asked of the L2).
-  // Every run taken is processed; the counter is read by whole warps.
-  int64_t run = map.take<false>(&next_run, lane);
-  int64_t rpf = (kPrefetch && run < runs) ? map.take<false>(&next_run, lane) : runs;
-  if (run < runs) shift_pipe_load<GT, NR>(x, run, lane, nvec, cur);
-  while (run < runs) {  // warp-uniform
-    int64_t rload;
-    if constexpr (kPrefetch) {
-      rload = rpf;
-      rpf = rload < runs ? map.take<false>(&next_run, lane) : runs;
-    } else {
-      rload = map.take<false>(&next_run, lane);
-    }
-    if (rload < runs) shift_pipe_load<GT, NR>(x, rload, lane, nvec, nxt);
-    if constexpr (kPrefetch) {
-      if (rpf < runs) shift_prefetch(x, rpf, lane, NR, nvec);
-    }
-    float g[8];
-    widen8<GT>(cur.r[0], g);
-#pragma unroll
-    for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
-    shift_down8(g, sh);
-    const int64_t gi = 1 + run * kRun + lane;
-    if (lane < kRun && gi < nvec - 1) {
-      float p[8] = {cur.s[0].x, cur.s[0].y, cur.s[0].z, cur.s[0].w, cur.s[1].x, cur.s[1].y, cur.s[1].z, cur.s[1].w};
-      float m[8] = {cur.s[2].x, cur.s[2].y, cur.s[2].z, cur.s[2].w, cur.s[3].x, cur.s[3].y, cur.s[3].z, cur.s[3].w};
-      float v[8] = {cur.s[4].x, cur.s[4].y, cur.s[4].z, cur.s[4].w, cur.s[5].x, cur.s[5].y, cur.s[5].z, cur.s[5].w};
-      shift_update<PT, WRITE_P16>(x, a.head + gi * kGroup, g, p, m, v, gs, bad);
-    }
-    cur = nxt;
-    run = rload;
-  }
-  shift_edges<GT, PT, WRITE_P16>(x, nvec, gs, bad);
-  if (a.nonfinite) {
-    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
-    if (any && lane == 0) *a.nonfinite = 1;
-  }
-}
-
-#ifndef SS_SHIFT_VEC_BATCH
-#define SS_SHIFT_VEC_BATCH 8  // rank chunks loaded per batch in the single-buffered form
-#endif
-#ifndef SS_SHIFT_VEC_THREADS
-#define SS_SHIFT_VEC_THREADS 512  // one block per SM: up to 128 registers
-#endif
-constexpr int kShiftVecBatch = SS_SHIFT_VEC_BATCH;
-constexpr int kShiftVecThreads = SS_SHIFT_VEC_THREADS;
-
-template <int GT, int PT, bool WRITE_P16, int MAXR>
-__global__ void __launch_bounds__(kShiftVecThreads, 1)
-    adam_shift_vec_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
-  __shared__ unsigned next_run;
-  if (threadIdx.x == 0) next_run = 0;
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  const StepArgs<MAXR>& a = x.s;
-  if (a.dev_skip != nullptr && *a.dev_skip != 0) return;
-  const float gs = a.dev_scale ? *a.dev_scale : 1.0f;
-  const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
-  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
-  const int sh = x.rphase[0] >> 1;
-  const int lane = threadIdx.x & 31;
-  const ChunkMap<kShiftVecThreads / 32> map(runs * 32);
-  const bool prefetch = a.n_ranks <= SS_SHIFT_VEC_PF_RANKS;
-  bool bad = false;
-  int64_t run = map.take<false>(&next_run, lane);
-  while (run < runs) {  // warp-uniform
-    const int64_t rn = map.take<false>(&next_run, lane);
-    if (prefetch && rn < runs) shift_prefetch(x, rn, lane, a.n_ranks, nvec);
-    const int64_t gi = 1 + run * kRun + lane;
-    const int64_t gl = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the array, unused
-    const int64_t el = a.head + gl * kGroup;
-    const bool body = lane < kRun && gi < nvec - 1;
-    const int64_t e = a.head + gi * kGroup;
-    // the group's state is requested with the first batch of rank chunks, so both arrive
-    // in one round trip; the ranks' chunks come in batches, all loads of a batch first
-    float4 s4[6];
-    float g[8];
-    for (int r0 = 0; r0 < a.n_ranks; r0 += kShiftVecBatch) {
-      uint4 w[kShiftVecBatch];
-#pragma unroll
-      for (int j = 0; j < kShiftVecBatch; ++j)
-        if (r0 + j < a.n_ranks)
-          w[j] = __ldcs(reinterpret_cast<const uint4*>(
-              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) - x.rphase[0]));
-      if (r0 == 0 && body) {
-        s4[0] = __ldcs(reinterpret_cast<const float4*>(a.master + e));
-        s4[1] = __ldcs(reinterpret_cast<const float4*>(a.master + e) + 1);
-        s4[2] = __ldcs(reinterpret_cast<const float4*>(a.m + e));
-        s4[3] = __ldcs(reinterpret_cast<const float4*>(a.m + e) + 1);
-        s4[4] = __ldcs(reinterpret_cast<const float4*>(a.v + e));
-        s4[5] = __ldcs(reinterpret_cast<const float4*>(a.v + e) + 1);
-      }
-#pragma unroll
-      for (int j = 0; j < kShiftVecBatch; ++j) {
-        if (r0 + j < a.n_ranks) {
-          if (r0 + j == 0) widen8<GT>(w[j], g);
-          else add8<GT>(w[j], g);
-        }
-      }
-    }
-    shift_down8(g, sh);
-    if (body) {
-      float p[8] = {s4[0].x, s4[0].y, s4[0].z, s4[0].w, s4[1].x, s4[1].y, s4[1].z, s4[1].w};
-      float m[8] = {s4[2].x, s4[2].y, s4[2].z, s4[2].w, s4[3].x, s4[3].y, s4[3].z, s4[3].w};
-      float v[8] = {s4[4].x, s4[4].y, s4[4].z, s4[4].w, s4[5].x, s4[5].y, s4[5].z, s4[5].w};
-      shift_update<PT, WRITE_P16>(x, e, g, p, m, v, gs, bad);
-    }
-    run = rn;
-  }
-  shift_edges<GT, PT, WRITE_P16>(x, nvec, gs, bad);
-  if (a.nonfinite) {
-    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
-    if (any && lane == 0) *a.nonfinite = 1;
-  }
-}
-
 // Splits a double into an fp32 pair hi + lo (hi = nearest float, lo = nearest float to the rest).
 void split(double x, float& hi, float& lo) {
   hi = static_cast<float>(x);
@@ -747,55 +294,6 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 enum class Path { kScalar, kVector, kPipe, kShift };
 
-template <int G, int P, bool W, int MAXR, int NR>
-ss_status launch_shift_pipe_n(const ShiftArgs<MAXR>& x, void* stream) {
-  auto* fn = adam_shift_pipe_kernel<G, P, W, MAXR, NR>;
-  constexpr int threads = ShiftShape<NR>::kThreadsPerBlock;
-  const int64_t runs = ((x.s.n - x.s.head) / kGroup - 2 + kRun - 1) / kRun;
-  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, threads), x, stream, threads);
-}
-
-template <int G, int P, bool W, int MAXR>
-ss_status launch_shift_vec(const ShiftArgs<MAXR>& x, void* stream) {
-  auto* fn = adam_shift_vec_kernel<G, P, W, MAXR>;
-  const int64_t runs = ((x.s.n - x.s.head) / kGroup - 2 + kRun - 1) / kRun;
-  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kShiftVecThreads), x, stream,
-                kShiftVecThreads);
-}
-
-template <int G, int P, bool F, bool W, int MAXR>
-ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t pphase, void* stream) {
-  ShiftArgs<MAXR> x;
-  std::memset(&x, 0, sizeof x);
-  x.s = a;
-  for (int32_t r = 0; r < a.n_ranks; ++r) x.rphase[r] = rphase[r];
-  x.pphase = pphase;
-  // 16-bit gradients all at one phase: the warp-cooperative forms (double-buffered up to 8
-  // ranks, single-buffered above)
-  bool same = true;
-  for (int32_t r = 1; r < a.n_ranks; ++r) same = same && rphase[r] == rphase[0];
-  if constexpr (!F) {
-    if (same) {
-      if constexpr (MAXR == kSmallRanks) {
-        switch (a.n_ranks) {
-          case 1: return launch_shift_pipe_n<G, P, W, MAXR, 1>(x, stream);
-          case 2: return launch_shift_pipe_n<G, P, W, MAXR, 2>(x, stream);
-          case 3: return launch_shift_pipe_n<G, P, W, MAXR, 3>(x, stream);
-          case 4: return launch_shift_pipe_n<G, P, W, MAXR, 4>(x, stream);
-          case 5: return launch_shift_pipe_n<G, P, W, MAXR, 5>(x, stream);
-          case 6: return launch_shift_pipe_n<G, P, W, MAXR, 6>(x, stream);
-          case 7: return launch_shift_pipe_n<G, P, W, MAXR, 7>(x, stream);
-          case 8: return launch_shift_pipe_n<G, P, W, MAXR, 8>(x, stream);
-          default: break;
-        }
-      }
-      return launch_shift_vec<G, P, W, MAXR>(x, stream);
-    }
-  }
-  auto* fn = adam_shift_kernel<G, P, F, W, MAXR>;
-  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup), x, stream);
-}
-
 template <int G, int P, bool W, int MAXR, int NR, bool F = false>
 ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
   auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
@@ -820,13 +318,13 @@ ss_status launch_pipe(const StepArgs<MAXR>& a, void* stream) {
 template <int MAXR>
 ss_status run_adam(const StepArgs<MAXR>& a, Path path, bool from_g32, bool p16, ss_dtype gt, ss_dtype pt,
                    const uint8_t* rphase, uint8_t pphase, void* stream) {
+  if (path == Path::kShift) return shift_step<MAXR>(a, gt, pt, from_g32, p16, rphase, pphase, stream);
   // Only reachable forms are instantiated: an fp32 gradient (gt is then the
   // placeholder SS_BF16) always travels with the small rank table and takes the
   // double-buffered, shifted or element-wise form; the double-buffered form is
   // chosen only for at most 8 ranks, so only with the small table.
 #define SS_ADAM_CASE(G, P, F, W)                                                          \
   if (gt == G && pt == P && from_g32 == F && p16 == W) {                                  \
-    if (path == Path::kShift) return launch_shift<G, P, F, W, MAXR>(a, rphase, pphase, stream); \
     if (path == Path::kPipe) {                                                            \
       if constexpr (MAXR != kSmallRanks) return SS_ERR_INVALID_ARG;                       \
       else if constexpr (F) return launch_pipe_n<G, P, W, MAXR, 2, true>(a, stream);      \

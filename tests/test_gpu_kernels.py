@@ -387,10 +387,10 @@ def test_step_split_calls_agree(ss):
 @pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
 @pytest.mark.parametrize("same", [True, False])
 def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
-    """Rank views off the aligned state's phase: all at one offset (1..7, the warp-cooperative
-    kernels: double-buffered for N <= 8, single-buffered for 9) or rank r at (r % 7) + 1 (mixed
-    phases: the per-thread kernel), from a 1-group body (n = 27) to many runs per warp; equal to
-    the aligned kernel bit for bit and to the oracle."""
+    """Rank views off the aligned state's phase: all at one offset (1..7) or rank r at (r % 7) + 1
+    (mixed phases: each rank shifted by its own phase), through the warp-cooperative kernels
+    (double-buffered for N <= 8, single-buffered for 9), from a 1-group body (n = 27) to many runs
+    per warp; equal to the aligned kernel bit for bit and to the oracle."""
     import torch
     hp = dict(HP, step=5)
     ref = _oracle_step(n, N, fmt, hp)
@@ -406,6 +406,29 @@ def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
         assert torch.equal(x, y)
     assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
     _check(*b, pb, ref, fmt)
+
+
+@pytest.mark.parametrize("N", [3, 8, 16, 65, 1024])
+def test_step_mixed_phases(ss, N):
+    """Rank r's gradient view r % 8 elements into its buffer (so some ranks sit on the state's
+    16-byte phase and the others at every other phase): the warp-cooperative kernels shift each
+    rank by its own phase before adding it in rank order -- double-buffered up to 8 ranks,
+    single-buffered above, both rank-table sizes; bit-equal to the aligned kernel and within the
+    tolerance of the oracle."""
+    import torch
+    n = 40_009
+    ref = _oracle_step(n, N, synth.BF16, HP)
+    G_al = [dev_bits(s, n) for s in ref[0]]
+    G_mx = [dev_bits(s, n, offset=r % 8) for r, s in enumerate(ref[0])]
+    a, b = _state(n), _state(n)
+    pa = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    pb = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(HP, n, *a, rank_grads=G_al, param16=pa)
+    ss.ss_adam_step(HP, n, *b, rank_grads=G_mx, param16=pb)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
+    _check(*b, pb, ref, synth.BF16)
 
 
 @pytest.mark.parametrize("N", [2, 8, 16])
