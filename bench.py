@@ -325,8 +325,8 @@ def run_e2e(u, steps: int, device, t_counter):
     flags = [torch.zeros(1, dtype=torch.int32, device=device) for _ in range(2)]
     host_out = [torch.full((1,), -1, dtype=torch.int32, pin_memory=True) for _ in range(2)]
     s_cmp, s_d2h = (torch.cuda.Stream(device) for _ in range(2))
-    # the gradients go in as 256 MB pieces spread over four copy streams: on the GB300 machine one
-    # stream of back-to-back pieces moved ~105 GB/s, four streams (or one 16 GB copy) ~210 GB/s
+    # the gradients go in as 256 MB pieces spread over four copy streams (measured on GB300:
+    # back-to-back pieces on one stream moved ~105 GB/s, four streams or one 16 GB copy ~210 GB/s)
     s_h2d = [torch.cuda.Stream(device) for _ in range(4)]
     piece = 256 << 20
     src_b = host_in.view(torch.uint8).view(-1)

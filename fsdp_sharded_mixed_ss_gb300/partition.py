@@ -39,7 +39,7 @@ from typing import Sequence
 
 import numpy as np
 
-from . import SS_BF16, SS_FP16, ss_adam_step, ss_flatten_layout, ss_shard_segments, ss_unshard
+from . import ss_adam_step, ss_flatten_layout, ss_shard_segments, ss_unshard
 
 
 @dataclass
@@ -148,5 +148,4 @@ def shard_step(hp: dict, part: Partition, full_grad16, master, m, v, shard16_pad
     ss_adam_step(hp, part.n, master, m, v, rank_grads=[rows[r] for r in range(part.world)],
                  post_scale=post_scale, param16=shard16_padded[:part.n], **step_options)
     gathered = gather_params(shard16_padded, part, out=gathered, group=group)
-    dt = SS_BF16 if str(flat.dtype).endswith("bfloat16") else SS_FP16
-    ss_unshard(gathered_rows(gathered, part), part.bounds, flat, dtype=dt)
+    ss_unshard(gathered_rows(gathered, part), part.bounds, flat)

@@ -99,6 +99,49 @@ def test_graph_capture_replays_the_clipped_step(ss):
     assert np.array_equal(graphed[1].view(torch.int16).cpu().numpy().view(np.uint16), m16)
 
 
+def test_graph_capture_replays_the_shifted_load_steps(ss):
+    """The shifted-load kernel forms -- 8 ranks one element off the state's phase (double-buffered,
+    one phase), 4 ranks at mixed phases (double-buffered, a shift per rank), 16 ranks off phase
+    (single-buffered) -- each take their runs from a counter in shared memory; captured once into a
+    CUDA graph and replayed 3 times, equal bit for bit to the same calls run eagerly 3 times."""
+    import torch
+    n = 1_000_003
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=2)
+    cases = [(8, lambda r: 1), (4, lambda r: (r % 7) + 1), (16, lambda r: 3)]
+    G = []
+    for N, off in cases:
+        views = []
+        for r in range(N):
+            base = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+            views.append(fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 5), base[off(r):off(r) + n]))
+        G.append(views)
+
+    def buffers():
+        return [[fill(synth.normal(0.02, synth.FP32, synth.MASTER, i), torch.empty(n, device="cuda")),
+                 torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda"),
+                 torch.empty(n, dtype=torch.bfloat16, device="cuda")] for i in range(len(cases))]
+
+    def step(bufs):
+        for views, b in zip(G, bufs):
+            ss.ss_adam_step(hp, n, *b[:3], rank_grads=views, param16=b[3])
+
+    eager = buffers()
+    for _ in range(3):
+        step(eager)
+    torch.cuda.synchronize()
+    graphed = buffers()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):      # the eager calls above warmed up the library
+        step(graphed)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, graphed):
+        for x, y in zip(a, b):
+            assert torch.equal(x, y)
+
+
 def test_two_streams_run_independent_shards_concurrently(ss):
     """Two shards stepped in alternation on two streams (no ordering between the streams) give the
     same bits as the same steps run one after another on one stream."""
