@@ -254,12 +254,23 @@ def test_step_from_fp32_grad_matches_fused(ss):
     assert torch.equal(p16.view(torch.int16), p2.view(torch.int16))
 
 
-def test_step_options(ss):
+@pytest.mark.parametrize("N,offsets", [
+    (4, lambda r: 0),            # aligned: the double-buffered kernel
+    (12, lambda r: 0),           # aligned: the single-buffered kernel
+    (2, lambda r: 1),            # one phase off: warp-cooperative double-buffered, 512-thread blocks
+    (8, lambda r: 3),            # one phase off: warp-cooperative double-buffered, 384-thread blocks
+    (4, lambda r: (r % 7) + 1),  # mixed phases: warp-cooperative double-buffered, a shift per rank
+    (12, lambda r: 5),           # one phase off: warp-cooperative single-buffered
+    (12, lambda r: (r % 7) + 1), # mixed phases, more ranks: the per-thread kernel
+])
+def test_step_options(ss, N, offsets):
+    """post_scale, g_out, the non-finite flag, the device gradient scale and the skip flag through
+    every form of the fused step kernel, against the oracle (g_out bit-exact)."""
     import torch
-    n, N = 30_001, 4
+    n = 30_001
     coef = np.float32(0.37)
     ref = _oracle_step(n, N, synth.BF16, HP, grad_scale=float(coef), post_scale=0.25)
-    G = [dev_bits(s, n) for s in ref[0]]
+    G = [dev_bits(s, n, offset=offsets(r)) for r, s in enumerate(ref[0])]
     master, m, v = _state(n)
     p16 = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
     g_out = torch.empty(n, dtype=torch.float32, device="cuda")
@@ -388,9 +399,10 @@ def test_step_split_calls_agree(ss):
 @pytest.mark.parametrize("same", [True, False])
 def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
     """Rank views off the aligned state's phase: all at one offset (1..7) or rank r at (r % 7) + 1
-    (mixed phases: each rank shifted by its own phase), through the warp-cooperative kernels
-    (double-buffered for N <= 8, single-buffered for 9), from a 1-group body (n = 27) to many runs
-    per warp; equal to the aligned kernel bit for bit and to the oracle."""
+    (mixed phases), from a 1-group body (n = 27) to many runs per warp: the warp-cooperative
+    double-buffered kernel up to 8 ranks (one sum shifted once, or each rank shifted by its own
+    phase), for 9 ranks the single-buffered one (one phase) or the per-thread one (mixed); equal
+    to the aligned kernel bit for bit and to the oracle."""
     import torch
     hp = dict(HP, step=5)
     ref = _oracle_step(n, N, fmt, hp)
@@ -411,10 +423,10 @@ def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
 @pytest.mark.parametrize("N", [3, 8, 16, 65, 1024])
 def test_step_mixed_phases(ss, N):
     """Rank r's gradient view r % 8 elements into its buffer (so some ranks sit on the state's
-    16-byte phase and the others at every other phase): the warp-cooperative kernels shift each
-    rank by its own phase before adding it in rank order -- double-buffered up to 8 ranks,
-    single-buffered above, both rank-table sizes; bit-equal to the aligned kernel and within the
-    tolerance of the oracle."""
+    16-byte phase and the others at every other phase): up to 8 ranks the warp-cooperative
+    double-buffered kernel shifts each rank by its own phase before adding it in rank order, more
+    ranks take the per-thread kernel (both rank-table sizes); bit-equal to the aligned kernel and
+    within the tolerance of the oracle."""
     import torch
     n = 40_009
     ref = _oracle_step(n, N, synth.BF16, HP)
