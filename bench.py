@@ -60,6 +60,9 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="instead of the benchmark line, time every kernel on the sweep and layer shapes")
     ap.add_argument("--suite-n", type=int, default=1 << 26, help="shard length of the --suite runs")
+    ap.add_argument("--suite-pad", type=int, default=0, metavar="ELEMS",
+                    help="allocate each rank's gradient buffer ELEMS elements longer than the shard (so the "
+                         "buffers do not sit at power-of-two distances from each other)")
     ap.add_argument("--suite-only", default=None, metavar="REGEX",
                     help="time only the --suite entries whose name matches (e.g. for a small ncu capture)")
     return ap.parse_args()
@@ -594,7 +597,7 @@ def run_suite(args, device) -> dict:
     def want(*names):
         return args.suite_only is None or any(re.search(args.suite_only, k) for k in names)
 
-    out = {"peak_hbm_gbs": measured_peaks()["hbm_gbs"], "n": args.suite_n}
+    out = {"peak_hbm_gbs": measured_peaks()["hbm_gbs"], "n": args.suite_n, "pad": args.suite_pad}
     n = args.suite_n
     hp = dict(lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=1000)
     st = []
@@ -620,7 +623,7 @@ def run_suite(args, device) -> dict:
             continue
         G = []
         for r in range(N):
-            t = torch.empty(n, dtype=torch.bfloat16, device=device)
+            t = torch.empty(n + args.suite_pad, dtype=torch.bfloat16, device=device)[:n]
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
             G.append(t)
         if want(f"adam_step_N{N}"):
@@ -675,7 +678,7 @@ def run_suite(args, device) -> dict:
         m7 = n - 7
         G = []
         for r in range(64):
-            t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
+            t = torch.empty(n + 8 + args.suite_pad, dtype=torch.bfloat16, device=device)
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
             G.append(t[offset(r):offset(r) + m7])
         by_ranks = {}
@@ -689,7 +692,7 @@ def run_suite(args, device) -> dict:
     if want("adam_step_by_ranks"):
         G = []
         for r in range(32):
-            t = torch.empty(n, dtype=torch.bfloat16, device=device)
+            t = torch.empty(n + args.suite_pad, dtype=torch.bfloat16, device=device)[:n]
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
             G.append(t)
         by_ranks = {}

@@ -294,6 +294,12 @@ bool valid_hp(const ss_adamw_hparams* hp) {
 
 enum class Path { kScalar, kVector, kPipe, kShift };
 
+// The rank counts (bit N set: N ranks) whose aligned steps take the warp-cooperative kernel.
+#ifndef SS_WARP_COOP_RANK_MASK
+#define SS_WARP_COOP_RANK_MASK ((1u << 4) | (1u << 5) | (0xFFu << 9))
+#endif
+constexpr unsigned kWarpCoopRankMask = SS_WARP_COOP_RANK_MASK;
+
 template <int G, int P, bool W, int MAXR, int NR, bool F = false>
 ss_status launch_pipe_n(const StepArgs<MAXR>& a, void* stream) {
   auto* fn = adam_pipe_kernel<G, P, F, W, MAXR, NR>;
@@ -429,6 +435,17 @@ ss_status ss_adam_step(const ss_adamw_hparams* hp, int64_t n, const float* g32, 
           rphase[r] = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(rank_grads[r]) + 2u * h) & 15u);
       if (param16) pphase = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(param16) + 2u * h) & 15u);
     }
+  }
+  // Some rank counts whose 16-bit arrays share the state's phase take the warp-cooperative
+  // double-buffered kernel of ss_step_shift.cu too, every phase 0 (same results). Measured
+  // on GB300 at 2^26 elements: 9-16 ranks 0.99-1.05 of the copy peak there, against
+  // 0.97-0.99 single-buffered here and 0.80-0.91 for this file's double-buffered kernel
+  // in 256-thread blocks; 5 ranks 1.00 against 0.96; 4 ranks 1.00 against 0.98.
+  if (vec && !from_g32 && n_ranks <= 16 && ((kWarpCoopRankMask >> n_ranks) & 1u) && n - h >= 3 * kGroup) {
+    path = Path::kShift;
+    for (int32_t r = 0; r < n_ranks; ++r)
+      rphase[r] = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(rank_grads[r]) + 2u * h) & 15u);
+    if (param16) pphase = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(param16) + 2u * h) & 15u);
   }
   const AdamConst k = make_const(*hp);
   auto fill = [&](auto& a) {

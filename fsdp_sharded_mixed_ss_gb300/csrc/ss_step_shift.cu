@@ -1,12 +1,14 @@
 // ss_step_shift.cu -- the fused shard step (ss_adam_step) when 16-bit arrays are
 // off the fp32 state's 16-byte phase: gradient views at boundaries that are not
-// multiples of 8 elements, or param16 inside a flat buffer at such a boundary.
-// Three kernel forms share the per-element arithmetic of ss_math.cuh: a
-// warp-cooperative double-buffered one for up to 8 ranks (at one phase, or
-// each rank shifted by its own phase), a warp-cooperative single-buffered one
-// for more ranks at one phase, and a per-thread one for more ranks at mixed
-// phases (or an fp32 gradient with param16 off phase). Each gradient byte is
-// loaded once in the warp-cooperative forms.
+// multiples of 8 elements, or param16 inside a flat buffer at such a boundary
+// (and, at phase 0, aligned gradients of 9-16 ranks, where the double-buffered
+// form here measured fastest). Three kernel forms share the per-element
+// arithmetic of ss_math.cuh: a warp-cooperative double-buffered one for up to
+// 16 ranks at one phase, or up to 8 with each rank shifted by its own phase; a
+// warp-cooperative single-buffered one for more ranks at one phase; and a
+// per-thread one for more ranks at mixed phases (or an fp32 gradient with
+// param16 off phase). Each gradient byte is loaded once in the
+// warp-cooperative forms.
 #include "ss_step.cuh"
 
 namespace ss {
@@ -181,11 +183,18 @@ constexpr int kRun = 31;  // groups per warp run
 #ifndef SS_SHIFT_VEC_PF_RANKS
 #define SS_SHIFT_VEC_PF_RANKS 13
 #endif
+// Above 8 ranks (one phase) two runs' chunks need up to ~215 registers: one 256-thread
+// block per SM (up to 255 registers). Measured on GB300 at 2^26 elements, 9-16 ranks one
+// element off phase: 0.99-1.05 of the copy peak, against 0.75-0.98 single-buffered.
+#ifndef SS_SHIFT_PIPE_MAX_RANKS
+#define SS_SHIFT_PIPE_MAX_RANKS 16
+#endif
 template <int NR>
 struct ShiftShape {
   static constexpr bool kNarrow = NR <= SS_SHIFT_NARROW_RANKS;
-  static constexpr int kThreadsPerBlock = kNarrow ? kChunkThreads : SS_SHIFT_WIDE_THREADS;
-  static constexpr int kBlocksPerSm = kNarrow ? kChunkBlocksPerSm : SS_SHIFT_WIDE_BLOCKS;
+  static constexpr bool kMany = NR > 8;
+  static constexpr int kThreadsPerBlock = kNarrow ? kChunkThreads : (kMany ? 256 : SS_SHIFT_WIDE_THREADS);
+  static constexpr int kBlocksPerSm = kNarrow ? kChunkBlocksPerSm : (kMany ? 1 : SS_SHIFT_WIDE_BLOCKS);
 };
 
 // One run's loads of one lane: the ranks' aligned 16-byte gradient chunks and
@@ -490,6 +499,19 @@ ss_status launch_shift_warp(const ShiftArgs<MAXR>& x, void* stream) {
       case 7: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 7>(x, stream);
       case 8: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 8>(x, stream);
       default: break;
+    }
+    if constexpr (!MIXED && SS_SHIFT_PIPE_MAX_RANKS > 8) {
+      switch (x.s.n_ranks) {
+        case 9: return launch_shift_pipe_n<G, P, W, false, MAXR, 9>(x, stream);
+        case 10: return launch_shift_pipe_n<G, P, W, false, MAXR, 10>(x, stream);
+        case 11: return launch_shift_pipe_n<G, P, W, false, MAXR, 11>(x, stream);
+        case 12: return launch_shift_pipe_n<G, P, W, false, MAXR, 12>(x, stream);
+        case 13: return launch_shift_pipe_n<G, P, W, false, MAXR, 13>(x, stream);
+        case 14: return launch_shift_pipe_n<G, P, W, false, MAXR, 14>(x, stream);
+        case 15: return launch_shift_pipe_n<G, P, W, false, MAXR, 15>(x, stream);
+        case 16: return launch_shift_pipe_n<G, P, W, false, MAXR, 16>(x, stream);
+        default: break;
+      }
     }
   }
   if constexpr (MIXED) return SS_ERR_INVALID_ARG;  // not reached: mixed phases take this form up to 8 ranks

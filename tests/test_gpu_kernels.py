@@ -161,11 +161,11 @@ def test_step_rank_counts(ss, N, goff, fmt):
 
 @pytest.mark.parametrize("gfmt,pfmt", [(synth.BF16, synth.FP16), (synth.FP16, synth.BF16), (synth.BF16, synth.BF16),
                                        (synth.FP16, synth.FP16), (synth.FP32, synth.FP16), (synth.FP32, synth.BF16)])
-@pytest.mark.parametrize("N,goff", [(3, 0), (9, 0), (3, 5)])
+@pytest.mark.parametrize("N,goff", [(3, 0), (9, 0), (20, 0), (3, 5)])
 def test_step_gradient_and_param_formats(ss, gfmt, pfmt, N, goff):
     """Every pairing of gradient format (bf16, fp16, or an fp32 gradient) with parameter format,
-    through the double-buffered (N = 3), single-buffered (N = 9) and shifted-load (views 5
-    elements off) kernels, against the oracle."""
+    through the double-buffered (N = 3), warp-cooperative (N = 9, aligned), single-buffered
+    (N = 20) and shifted-load (views 5 elements off) kernels, against the oracle."""
     import torch
     n = 30_011
     hp = dict(HP, step=7)
@@ -194,14 +194,14 @@ def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("N,from_g32", [(1, False), (2, True), (5, False), (8, False)])
+@pytest.mark.parametrize("N,from_g32", [(1, False), (2, True), (6, False), (8, False), (24, False)])
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, -2049), (2, 255), (3, 4103)])
 def test_step_chunk_boundaries(ss, N, from_g32, k, d):
     """Shard lengths around whole passes of the grid over its chunks (a pass: 16 chunks of 32
     8-element groups per block, one block per SM), so the last pass is just full, just short or
     just over, through each way the step kernels own chunks: adjacent per block (1 rank, an fp32
-    gradient), round robin (5 ranks: single-buffered kernel; 8 ranks: double-buffered). Every
-    element is stepped exactly once: all of the state against the oracle."""
+    gradient), round robin (6 and 24 ranks: single-buffered kernel; 8 ranks: double-buffered).
+    Every element is stepped exactly once: all of the state against the oracle."""
     import torch
     n = k * _sms() * 16 * 32 * 8 + d
     ref = _oracle_step(n, N, synth.BF16, HP)
@@ -443,16 +443,16 @@ def test_step_mixed_phases(ss, N):
     _check(*b, pb, ref, synth.BF16)
 
 
-@pytest.mark.parametrize("N", [2, 8, 16])
-@pytest.mark.parametrize("warps_per_sm", [12, 16])
+@pytest.mark.parametrize("N", [2, 8, 16, 32])
+@pytest.mark.parametrize("warps_per_sm", [8, 12, 16])
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, 7), (3, -5)])
 def test_step_shifted_run_boundaries(ss, N, warps_per_sm, k, d):
     """The warp-cooperative shifted-load kernels take runs of 31 groups from a per-block counter;
-    their grid passes over k x (SMs x resident warps) runs (12 or 16 warps per SM, by block shape),
-    so shard lengths whose body is just a whole number of passes, or one run more or less, check
-    that every run is taken exactly once (2 and 8 ranks: double-buffered; 16: single-buffered),
-    with the gradient views one element off the state's phase: all of the state against the
-    oracle, and bit-equal to the aligned kernel."""
+    their grid passes over k x (SMs x resident warps) runs (16, 12 or 8 warps per SM, by block
+    shape), so shard lengths whose body is just a whole number of passes, or one run more or less,
+    check that every run is taken exactly once (2, 8 and 16 ranks: double-buffered in 512-, 384-
+    and 256-thread blocks; 32: single-buffered), with the gradient views one element off the
+    state's phase: all of the state against the oracle, and bit-equal to the aligned kernel."""
     import torch
     runs = k * _sms() * warps_per_sm + d
     n = (runs * 31 + 2) * 8 + 3          # body groups 1 .. nvec - 2, plus a 3-element tail
