@@ -189,6 +189,13 @@ constexpr int kRun = 31;  // groups per warp run
 #ifndef SS_SHIFT_PIPE_MAX_RANKS
 #define SS_SHIFT_PIPE_MAX_RANKS 16
 #endif
+// Up to this many ranks at mixed phases take the double-buffered warp-cooperative kernel
+// (measured on GB300 at 2^26 elements with 16 allowed: 9 ranks 0.82 of the copy peak against
+// 0.73 per-thread, but 12 and 16 ranks 0.67 and 0.62 against 0.77 and 0.81 -- there the
+// per-rank shifts cost more issue slots than the update itself).
+#ifndef SS_SHIFT_MIXED_MAX_RANKS
+#define SS_SHIFT_MIXED_MAX_RANKS 8
+#endif
 template <int NR>
 struct ShiftShape {
   static constexpr bool kNarrow = NR <= SS_SHIFT_NARROW_RANKS;
@@ -500,21 +507,21 @@ ss_status launch_shift_warp(const ShiftArgs<MAXR>& x, void* stream) {
       case 8: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 8>(x, stream);
       default: break;
     }
-    if constexpr (!MIXED && SS_SHIFT_PIPE_MAX_RANKS > 8) {
+    if constexpr ((MIXED ? SS_SHIFT_MIXED_MAX_RANKS : SS_SHIFT_PIPE_MAX_RANKS) > 8) {
       switch (x.s.n_ranks) {
-        case 9: return launch_shift_pipe_n<G, P, W, false, MAXR, 9>(x, stream);
-        case 10: return launch_shift_pipe_n<G, P, W, false, MAXR, 10>(x, stream);
-        case 11: return launch_shift_pipe_n<G, P, W, false, MAXR, 11>(x, stream);
-        case 12: return launch_shift_pipe_n<G, P, W, false, MAXR, 12>(x, stream);
-        case 13: return launch_shift_pipe_n<G, P, W, false, MAXR, 13>(x, stream);
-        case 14: return launch_shift_pipe_n<G, P, W, false, MAXR, 14>(x, stream);
-        case 15: return launch_shift_pipe_n<G, P, W, false, MAXR, 15>(x, stream);
-        case 16: return launch_shift_pipe_n<G, P, W, false, MAXR, 16>(x, stream);
+        case 9: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 9>(x, stream);
+        case 10: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 10>(x, stream);
+        case 11: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 11>(x, stream);
+        case 12: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 12>(x, stream);
+        case 13: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 13>(x, stream);
+        case 14: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 14>(x, stream);
+        case 15: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 15>(x, stream);
+        case 16: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 16>(x, stream);
         default: break;
       }
     }
   }
-  if constexpr (MIXED) return SS_ERR_INVALID_ARG;  // not reached: mixed phases take this form up to 8 ranks
+  if constexpr (MIXED) return SS_ERR_INVALID_ARG;  // not reached: mixed phases take the double-buffered form only
   else return launch_shift_vec<G, P, W, MAXR>(x, stream);
 }
 
@@ -536,7 +543,7 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
     for (int32_t r = 1; r < a.n_ranks; ++r) same = same && rphase[r] == rphase[0];
     if (same) return launch_shift_warp<G, P, W, false, MAXR>(x, stream);
     if constexpr (MAXR == kSmallRanks) {
-      if (a.n_ranks <= 8) return launch_shift_warp<G, P, W, true, MAXR>(x, stream);
+      if (a.n_ranks <= SS_SHIFT_MIXED_MAX_RANKS) return launch_shift_warp<G, P, W, true, MAXR>(x, stream);
     }
   }
   // more ranks at mixed phases, or an fp32 gradient with param16 off phase: the per-thread form
