@@ -619,6 +619,7 @@ def run_suite(args, device) -> dict:
         off = f"adam_step_N{N}_grads_off_by_one"
         mixed = f"adam_step_N{N}_grads_mixed_phase"
         if not want(f"adam_step_N{N}", f"grad_reduce_N{N}", f"grad_sumsq_N{N}", off, mixed,
+                    f"grad_reduce_N{N}_grads_off_by_one", f"grad_sumsq_gout_N{N}_grads_off_by_one",
                     *(extra8 if N == 8 else ())):
             continue
         G = []
@@ -633,6 +634,16 @@ def run_suite(args, device) -> dict:
             out[f"grad_reduce_N{N}"] = entry(timed(lambda: ss.ss_grad_reduce(G, n, g32)), (2 * N + 4) * n)
         if want(f"grad_sumsq_N{N}"):
             out[f"grad_sumsq_N{N}"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, rank_grads=G)), 2 * N * n)
+        if want(f"grad_reduce_N{N}_grads_off_by_one", f"grad_sumsq_gout_N{N}_grads_off_by_one"):
+            # the gradient views one element off the fp32 output's 16-byte phase
+            Gm = [g[1:] for g in G]
+            m1 = n - 1
+            if want(f"grad_reduce_N{N}_grads_off_by_one"):
+                out[f"grad_reduce_N{N}_grads_off_by_one"] = entry(
+                    timed(lambda: ss.ss_grad_reduce(Gm, m1, g32[:m1])), (2 * N + 4) * m1)
+            if want(f"grad_sumsq_gout_N{N}_grads_off_by_one"):
+                out[f"grad_sumsq_gout_N{N}_grads_off_by_one"] = entry(
+                    timed(lambda: ss.ss_grad_sumsq(m1, acc, ws, rank_grads=Gm, g_out=g32[:m1])), (2 * N + 4) * m1)
         if want(off):
             # gradient views one element off the state's 16-byte phase: the shifted-load kernels
             Gm = [g[1:] for g in G]

@@ -216,6 +216,46 @@ __device__ __forceinline__ uint4 window16(const uint4& c0, const uint4& c1) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// ------------------------------------------------------------------ warp-cooperative shifted loads
+//
+// A 16-bit array whose 8-element groups do not start on 16-byte boundaries
+// (a view at an offset that is not a multiple of 8 elements) is read by whole
+// warps: a warp takes runs of kRun consecutive groups; lane j loads the aligned
+// 16-byte chunk under the start of group j of the run (lane 31 the one under
+// the group after the run), the lanes combine their chunks element by element
+// as the caller needs (e.g. the ranks' fp32 sum), and each lane then moves its
+// group's 8 values into place, taking the ones past its own chunk from the
+// next lane by shuffle. Each byte is loaded once.
+constexpr int kRun = 31;  // groups per warp run
+
+// c <- elements SH .. SH + 7 of the 16 values (this lane's c, the next lane's c),
+// in place: only the SH values that come from the next lane are shuffled, and
+// they are taken before c is moved down (all lanes of the warp call it with
+// the same SH).
+template <int SH>
+__device__ __forceinline__ void shift_down8(float (&c)[8]) {
+  float d[SH > 0 ? SH : 1];
+#pragma unroll
+  for (int j = 0; j < SH; ++j) d[j] = __shfl_down_sync(0xFFFFFFFFu, c[j], 1);
+#pragma unroll
+  for (int i = 0; i + SH < 8; ++i) c[i] = c[i + SH];
+#pragma unroll
+  for (int j = 0; j < SH; ++j) c[8 - SH + j] = d[j];
+}
+
+__device__ __forceinline__ void shift_down8(float (&g)[8], int sh) {
+  switch (sh) {  // warp-uniform
+    case 0: break;
+    case 1: shift_down8<1>(g); break;
+    case 2: shift_down8<2>(g); break;
+    case 3: shift_down8<3>(g); break;
+    case 4: shift_down8<4>(g); break;
+    case 5: shift_down8<5>(g); break;
+    case 6: shift_down8<6>(g); break;
+    default: shift_down8<7>(g); break;
+  }
+}
+
 // ------------------------------------------------------------------ work division
 //
 // The step and reduce kernels run one wave of blocks, one per SM. A chunk is 32

@@ -21,7 +21,7 @@ namespace {
 // writes ONE double per tile into the caller's workspace (GB300's fp64 rate is
 // low, so fp64 is kept to one value per tile). The head/tail elements (< 16)
 // get a slot of their own. A second one-block kernel adds the slots in a fixed
-// order. The partition depends only on n and the arrays' 16-byte phase, never
+// order. The partition depends only on n and the arrays' 16-byte phases, never
 // on the grid size, so the result is bit-reproducible.
 //
 // Error: each 8-element fp32 chain of non-negative terms is within 8 * 2^-24
@@ -95,7 +95,13 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
                                             bool& bad) {
   if (a.g_out) {
     if constexpr (VEC) {
-      st8f(a.g_out + e, g);
+      // g_out may sit off the inputs' 16-byte phase (then element by element)
+      if ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) == 0) {
+        st8f(a.g_out + e, g);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
@@ -376,8 +382,18 @@ ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_g
     ranges.push_back(rng(nonfinite_flag, 4, true));
   }
   if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
-  const int h = common_phase(p16, p32);
-  const bool vec = h >= 0 && h < n;
+  int h = common_phase(p16, p32);
+  bool vec = h >= 0 && h < n;
+  if (!vec && g_out) {
+    // the inputs at one phase and g_out at another: the groups follow the inputs (16-byte
+    // loads) and g_out is written element by element (it was the last array listed)
+    const std::vector<uintptr_t> in32(p32.begin(), p32.end() - 1);
+    const int hin = common_phase(p16, in32);
+    if (hin >= 0 && hin < n) {
+      h = hin;
+      vec = true;
+    }
+  }
   const int64_t head = vec ? h : 0;
   const int64_t nvec = (n - head) / kGroup;
   const int64_t ntiles = (nvec + kThreads * kSumsqGroups - 1) / (kThreads * kSumsqGroups);

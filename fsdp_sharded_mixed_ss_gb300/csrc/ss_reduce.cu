@@ -1,6 +1,9 @@
 // ss_reduce.cu -- the standalone virtual-rank gradient reduce (ss_grad_reduce):
 // the fp32 rank-ordered sum of the ranks' 16-bit gradient shards, optionally
-// scaled, accumulated into the output and checked for non-finite values.
+// scaled, accumulated into the output and checked for non-finite values. Three
+// forms: 16-byte vectors when the ranks and the output share a 16-byte phase,
+// warp-cooperative shifted loads when the ranks share a phase that is not the
+// output's, element-wise otherwise.
 #include "ss_common.cuh"
 
 namespace ss {
@@ -92,6 +95,102 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
   }
 }
 
+// Rank gradients all at one 16-byte phase that is not the fp32 output's (views
+// at an offset that is not a multiple of 8 elements into per-rank buffers,
+// with the output allocated per shard): warp-cooperative runs of kRun groups
+// (ss_common.cuh), the ranks' chunks loaded in batches of 8 and summed in rank
+// order before the shift, so each gradient byte is loaded once; the output
+// (and its old value when accumulating) stays in aligned 16-byte vectors.
+// Groups 0 and nvec - 1 and the head/tail elements go one by one.
+template <int MAXR>
+struct ShiftReduceArgs {
+  ReduceArgs<MAXR> s;
+  int32_t rphase;  // byte offset of the ranks' group starts past a 16-byte boundary (even, nonzero)
+};
+
+template <int GT, int MAXR>
+__global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_kernel(const __grid_constant__ ShiftReduceArgs<MAXR> x) {
+  __shared__ unsigned next_run;
+  if (threadIdx.x == 0) next_run = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const ReduceArgs<MAXR>& a = x.s;
+  const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
+  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
+  const int sh = x.rphase >> 1;
+  const int lane = threadIdx.x & 31;
+  const ChunkMap<kReduceChunkThreads / 32> map(runs * 32);  // one "chunk" per run
+  bool bad = false;
+  for (int64_t run = map.take<false>(&next_run, lane); run < runs; run = map.take<false>(&next_run, lane)) {
+    const int64_t gi = 1 + run * kRun + lane;
+    const int64_t gl = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the arrays, unused
+    const int64_t el = a.head + gl * kGroup;
+    float g[8];
+    for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
+      uint4 w[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (r0 + j < a.n_ranks)
+          w[j] = __ldcs(reinterpret_cast<const uint4*>(
+              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) - x.rphase));
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (r0 + j < a.n_ranks) {
+          if (r0 + j == 0) widen8<GT>(w[j], g);
+          else add8<GT>(w[j], g);
+        }
+      }
+    }
+    shift_down8(g, sh);
+    if (lane < kRun && gi < nvec - 1) {
+      const int64_t e = a.head + gi * kGroup;
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      }
+      if (a.accumulate) {
+        float o[8];
+        ld8f(a.out + e, o);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) g[j] = o[j] + g[j];
+      }
+      if (a.nonfinite) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+      }
+      st8f(a.out + e, g);
+    }
+  }
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t lo_end = a.head + kGroup, hi_start = a.head + (nvec - 1) * kGroup;
+  const int64_t n_edge = lo_end + (a.n - hi_start);
+  if (tid < n_edge) reduce_one<GT>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && lane == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int MAXR>
+ss_status run_reduce_shift(const ReduceArgs<MAXR>& a, int rphase, ss_dtype gt, void* stream) {
+  ShiftReduceArgs<MAXR> x;
+  std::memset(&x, 0, sizeof x);
+  x.s = a;
+  x.rphase = rphase;
+  const int64_t runs = ((a.n - a.head) / kGroup - 2 + kRun - 1) / kRun;
+#define SS_REDS_CASE(G)                                                                              \
+  if (gt == G) {                                                                                     \
+    auto* fn = reduce_shift_kernel<G, MAXR>;                                                         \
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kReduceChunkThreads), x, stream, \
+                  kReduceChunkThreads);                                                              \
+  }
+  SS_REDS_CASE(SS_BF16)
+  SS_REDS_CASE(SS_FP16)
+#undef SS_REDS_CASE
+  return SS_ERR_DTYPE;
+}
+
 template <int MAXR>
 ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* stream) {
 #define SS_RED_CASE(G)                                                                     \
@@ -140,12 +239,23 @@ ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtyp
   p32.push_back(reinterpret_cast<uintptr_t>(g_out));
   const int h = common_phase(p16, p32);
   const bool vec = h >= 0 && h < n;
+  // the ranks at one phase, the output at another: groups aligned for the output, the
+  // ranks read by the warp-cooperative shifted loads
+  int64_t head = vec ? h : 0;
+  int rphase = 0;
+  if (!vec && common_phase(p16, {}) >= 0) {
+    const int h32 = common_phase({}, p32);
+    if (h32 >= 0 && n - h32 >= 3 * kGroup) {
+      head = h32;
+      rphase = static_cast<int>((reinterpret_cast<uintptr_t>(rank_grads[0]) + 2u * h32) & 15u);
+    }
+  }
   auto fill = [&](auto& a) {
     for (int32_t r = 0; r < n_ranks; ++r) a.ranks.p[r] = rank_grads[r];
     a.out = g_out;
     a.nonfinite = nonfinite_flag;
     a.n = n;
-    a.head = vec ? h : 0;
+    a.head = head;
     a.n_ranks = n_ranks;
     a.post_scale = post_scale;
     a.accumulate = accumulate != 0;
@@ -154,12 +264,12 @@ ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtyp
     ReduceArgs<kSmallRanks> a;
     std::memset(&a, 0, sizeof a);
     fill(a);
-    return run_reduce(a, vec, gdtype, stream);
+    return rphase ? run_reduce_shift(a, rphase, gdtype, stream) : run_reduce(a, vec, gdtype, stream);
   }
   ReduceArgs<kLargeRanks> a;
   std::memset(&a, 0, sizeof a);
   fill(a);
-  return run_reduce(a, vec, gdtype, stream);
+  return rphase ? run_reduce_shift(a, rphase, gdtype, stream) : run_reduce(a, vec, gdtype, stream);
 }
 
 }  // extern "C"

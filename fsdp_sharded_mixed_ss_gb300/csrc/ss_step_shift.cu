@@ -164,7 +164,6 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
 // ranks 0.99 of the copy peak; 9-12 ranks only 0.77-0.82 -- one batch of 8
 // and a short second one, where the update's issue time is no longer hidden
 // behind memory).
-constexpr int kRun = 31;  // groups per warp run
 
 #ifndef SS_SHIFT_NARROW_RANKS
 #define SS_SHIFT_NARROW_RANKS 3  // up to this many ranks: one 512-thread block per SM (128 registers)
@@ -255,34 +254,6 @@ __device__ __forceinline__ void shift_prefetch(const ShiftArgs<MAXR>& x, int64_t
     const int k = lane - n_ranks;
     prefetch_l2((k == 0 ? a.master : (k == 1 ? a.m : a.v)) + a.head + g0 * kGroup,
                 static_cast<uint32_t>((gb - g0 + 1) * 32));
-  }
-}
-
-// c <- elements SH .. SH + 7 of the 16 values (this lane's c, the next lane's c),
-// in place: only the SH values that come from the next lane are shuffled, and
-// they are taken before c is moved down (all lanes of the warp call it with
-// the same SH).
-template <int SH>
-__device__ __forceinline__ void shift_down8(float (&c)[8]) {
-  float d[SH > 0 ? SH : 1];
-#pragma unroll
-  for (int j = 0; j < SH; ++j) d[j] = __shfl_down_sync(0xFFFFFFFFu, c[j], 1);
-#pragma unroll
-  for (int i = 0; i + SH < 8; ++i) c[i] = c[i + SH];
-#pragma unroll
-  for (int j = 0; j < SH; ++j) c[8 - SH + j] = d[j];
-}
-
-__device__ __forceinline__ void shift_down8(float (&g)[8], int sh) {
-  switch (sh) {  // warp-uniform
-    case 0: break;
-    case 1: shift_down8<1>(g); break;
-    case 2: shift_down8<2>(g); break;
-    case 3: shift_down8<3>(g); break;
-    case 4: shift_down8<4>(g); break;
-    case 5: shift_down8<5>(g); break;
-    case 6: shift_down8<6>(g); break;
-    default: shift_down8<7>(g); break;
   }
 }
 
