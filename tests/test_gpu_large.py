@@ -2,7 +2,9 @@
 
 n = 2^31 + 7 elements, N = 2 bf16 ranks (about 39 GB on the device): one fused step, checked on
 sampled elements (both ends, runs around 2^31 and random points) against the oracle; then the
-16-bit parameters unsharded with a 2^31 + 7-element shard and a small one, checked the same way.
+16-bit parameters unsharded with a 2^31 + 7-element shard and a small one, checked the same way;
+and the same step with both ranks' gradient views one element off the state's 16-byte phase (the
+warp-cooperative shifted-load kernel, whose run and group indices then pass 2^31 too).
 """
 import numpy as np
 import pytest
@@ -66,3 +68,37 @@ def test_step_and_unshard_beyond_2_31(ss):
     fi = torch.from_numpy(np.concatenate([idx, n + np.arange(1000)]).astype(np.int64)).cuda()
     want = torch.cat([p16[it], small])
     assert torch.equal(flat[fi].view(torch.int16), want.view(torch.int16))
+
+
+def test_shifted_step_beyond_2_31_elements(ss):
+    import torch
+    n, N = (1 << 31) + 7, 2
+    hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1)
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1) for r in range(N)]
+    G = []
+    for s in specs:
+        base = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+        v = base[1:n + 1]
+        synth.device_fill(s, v.view(torch.int16))
+        G.append(v)
+    mspec = synth.normal(0.02, synth.FP32, synth.MASTER)
+    master = torch.empty(n, dtype=torch.float32, device="cuda")
+    synth.device_fill(mspec, master.view(torch.int32))
+    m = torch.zeros(n, dtype=torch.float32, device="cuda")
+    v = torch.zeros(n, dtype=torch.float32, device="cuda")
+    p16 = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    ss.ss_adam_step(hp, n, master, m, v, rank_grads=G, param16=p16)
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([sample_indices(0, n, 200_000, 6),
+                                    np.arange((1 << 31) - 40, (1 << 31) + 7)]))
+    g = oracle.grad_reduce([synth.host_gather(s, idx) for s in specs], oracle.BF16)
+    om = synth.host_gather(mspec, idx).view(np.float32).copy()
+    omm, ov = np.zeros(idx.size, np.float32), np.zeros(idx.size, np.float32)
+    rp = oracle.adamw(hp["lr"], hp["beta1"], hp["beta2"], hp["eps"], hp["weight_decay"], 1, g, om, omm, ov,
+                      p16_dtype=oracle.BF16)
+    it = torch.from_numpy(idx.astype(np.int64)).cuda()
+    for name, t, r in (("master", master, om), ("m", m, omm), ("v", v, ov)):
+        assert_state_close(t[it].cpu().numpy(), r, name)
+    assert_p16_within_ulp(p16.view(torch.int16)[it].cpu().numpy().view(np.uint16), rp, oracle.BF16, "p16")
+    del G, master, m, v, p16
+    torch.cuda.empty_cache()
