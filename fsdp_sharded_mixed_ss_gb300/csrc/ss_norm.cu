@@ -86,26 +86,70 @@ __device__ __forceinline__ float reduced1(const SumsqArgs<MAXR>& a, int64_t e) {
   return g;
 }
 
+// g (this lane's group at element e) stored to g_out when g_out is K floats past
+// a 16-byte boundary at the group's start: the lane writes the two aligned
+// float4 vectors that start inside its group -- elements 4-K..7-K, and 8-K..7
+// followed by the next lane's first 4-K, taken by shuffle -- so the lanes of a
+// warp, which hold consecutive groups, cover their elements with aligned
+// stores; lane 0 writes its first 4-K elements one by one, and a lane whose
+// next lane has no group (lane 31, or the shard's last group) its last K.
+// All lanes call it (the shuffles); `valid` says the lane holds a group.
+template <int K>
+__device__ __forceinline__ void store_g_out_shifted(float* out, const float (&g)[8], bool valid, bool next_valid) {
+  static_assert(K >= 1 && K <= 3, "an fp32 array is 1-3 floats off a 16-byte boundary");
+  const int lane = threadIdx.x & 31;
+  float nx[4 - K];
+#pragma unroll
+  for (int j = 0; j < 4 - K; ++j) nx[j] = __shfl_down_sync(0xFFFFFFFFu, g[j], 1);
+  if (!valid) return;
+  __stcs(reinterpret_cast<float4*>(out + 4 - K), make_float4(g[4 - K], g[5 - K], g[6 - K], g[7 - K]));
+  if (lane < 31 && next_valid) {
+    float w[4];
+#pragma unroll
+    for (int j = 0; j < K; ++j) w[j] = g[8 - K + j];
+#pragma unroll
+    for (int j = 0; j < 4 - K; ++j) w[K + j] = nx[j];
+    __stcs(reinterpret_cast<float4*>(out + 8 - K), make_float4(w[0], w[1], w[2], w[3]));
+  } else {
+#pragma unroll
+    for (int j = 0; j < K; ++j) out[8 - K + j] = g[8 - K + j];
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 4 - K; ++j) out[j] = g[j];
+  }
+}
+
+// How g_out is written: as 16-byte vectors at the inputs' phase, realigned
+// between lanes by store_g_out_shifted (g_out 1-3 floats off that phase), or
+// element by element.
+enum GoutStore : int { kGoutVec = 0, kGoutShuffle = 1, kGoutElem = 2 };
+
 // One reduced group of 8 values at element e: optionally stored to g_out, its
 // squares added in fp32 (a fixed FMA chain), and the sum added to the thread's
 // fp32 pair. The finiteness test runs per element only when the group's sum is
-// not finite (a non-finite value, or squares past the fp32 range).
-template <bool VEC, int MAXR>
+// not finite (a non-finite value, or squares past the fp32 range). With
+// kGoutShuffle all lanes of the warp call it, `valid` telling which hold a
+// group; otherwise only lanes holding a group call it.
+template <bool VEC, int GOUT, int MAXR>
 __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e, const float (&g)[8], dd& s,
-                                            bool& bad) {
+                                            bool& bad, bool valid = true, bool next_valid = true) {
   if (a.g_out) {
-    if constexpr (VEC) {
-      // g_out may sit off the inputs' 16-byte phase (then element by element)
-      if ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) == 0) {
-        st8f(a.g_out + e, g);
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
+    if constexpr (GOUT == kGoutShuffle) {
+      switch ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) >> 2) {  // the same for every group
+        case 1: store_g_out_shifted<1>(a.g_out + e, g, valid, next_valid); break;
+        case 2: store_g_out_shifted<2>(a.g_out + e, g, valid, next_valid); break;
+        default: store_g_out_shifted<3>(a.g_out + e, g, valid, next_valid); break;
       }
+    } else if constexpr (VEC && GOUT == kGoutVec) {
+      st8f(a.g_out + e, g);
     } else {
 #pragma unroll
       for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
     }
+  }
+  if constexpr (GOUT == kGoutShuffle) {
+    if (!valid) return;
   }
   float c = 0.0f;
 #pragma unroll
@@ -125,7 +169,7 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
 // tile is in flight across the tile's block reduction. Batches past the end
 // (of the shard or of the block's tiles) read group 0 instead, always in
 // range, and are dropped, so no branch stands between the loads.
-template <int GT, int MAXR, int NR>
+template <int GT, int MAXR, int NR, int GOUT>
 __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, float2* red, bool& bad) {
   constexpr int kB = NR == 2 ? 4 : (NR <= 4 ? 2 : 1);  // groups per batch (measured best on GB300)
   static_assert(kSumsqGroups % (2 * kB) == 0, "two batches per pipeline round");
@@ -155,7 +199,9 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
         for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
       }
       const int64_t gq = g0 + (q0 + b) * kThreads;
-      if (gq < nvec) sumsq_group<true>(a, a.head + gq * kGroup, g, s, bad);
+      if constexpr (GOUT == kGoutShuffle)
+        sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad, gq < nvec, gq + 1 < nvec);
+      else if (gq < nvec) sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad);
     }
   };
   int64_t tile = blockIdx.x;
@@ -184,7 +230,7 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
 // constant (N <= 8), pipelined as above; NR == 0: any rank count, an fp32
 // gradient, or element-wise access -- each thread issues its tile's loads
 // group by group, then squares and sums them.
-template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR>
+template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR, int GOUT = kGoutVec>
 __global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
   __shared__ float2 red[2 * (kThreads / 32)];
   pdl_wait();
@@ -192,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_cons
   const int64_t nvec = (a.n - a.head) / kGroup;
   bool bad = false;
   if constexpr (VEC && !FROM_G32 && NR > 0) {
-    sumsq_ranked_tiles<GT, MAXR, NR>(a, red, bad);
+    sumsq_ranked_tiles<GT, MAXR, NR, GOUT>(a, red, bad);
   } else {
     int it = 0;
     for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
@@ -224,7 +270,9 @@ __global__ void __launch_bounds__(kThreads) sumsq_tiles_kernel(const __grid_cons
 #pragma unroll
       for (int q = 0; q < kSumsqGroups; ++q) {
         const int64_t gi = g0 + q * kThreads;
-        if (gi < nvec) sumsq_group<VEC>(a, a.head + gi * kGroup, g[q], s, bad);
+        if constexpr (GOUT == kGoutShuffle)
+          sumsq_group<VEC, GOUT>(a, a.head + gi * kGroup, g[q], s, bad, gi < nvec, gi + 1 < nvec);
+        else if (gi < nvec) sumsq_group<VEC, GOUT>(a, a.head + gi * kGroup, g[q], s, bad);
       }
       const double t = block_sum(s, red, it);
       if (threadIdx.x == 0) a.partials[tile] = t;
@@ -304,8 +352,13 @@ __global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, fl
   if (norm_out) *norm_out = norm;
 }
 
-template <int MAXR>
-ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
+// SH: g_out 1-3 floats off the inputs' phase (vector forms only): the per-rank-count
+// tiles realign it between lanes (measured on GB300 at 2^26 elements with the gradients
+// one element off: 2 ranks 0.82 of the copy peak against 0.29 element by element, 8 ranks
+// 0.91 against 0.72), the general tiles write it element by element (64 ranks: 0.87,
+// against 0.72 realigned).
+template <int MAXR, bool SH>
+ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
   // One wave: no more blocks than fit on the GPU at once (the kernel's own
   // occupancy), so every block takes the same number of tiles within one and
   // none waits for a free slot while the others finish.
@@ -316,8 +369,10 @@ ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype 
     launched = launch(fn, grid, a, stream);
   };
   const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
+  constexpr int kRanked = SH ? kGoutShuffle : kGoutVec;
+  constexpr int kGeneral = SH ? kGoutElem : kGoutVec;
 #define SS_SUMSQ_NR(G, R) \
-  case R: go(sumsq_tiles_kernel<G, false, true, MAXR, R>); break;
+  case R: go(sumsq_tiles_kernel<G, false, true, MAXR, R, kRanked>); break;
 // The per-rank-count forms exist for the small rank table only (at most 8 ranks),
 // and an fp32 gradient always travels with the small table.
 #define SS_SUMSQ_RANKED(G)                                                                              \
@@ -325,14 +380,14 @@ ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype 
     switch (nr) {                                                                                       \
       SS_SUMSQ_NR(G, 1) SS_SUMSQ_NR(G, 2) SS_SUMSQ_NR(G, 3) SS_SUMSQ_NR(G, 4)                           \
       SS_SUMSQ_NR(G, 5) SS_SUMSQ_NR(G, 6) SS_SUMSQ_NR(G, 7) SS_SUMSQ_NR(G, 8)                           \
-      default: go(sumsq_tiles_kernel<G, false, true, MAXR, 0>);                                         \
+      default: go(sumsq_tiles_kernel<G, false, true, MAXR, 0, kGeneral>);                               \
     }                                                                                                   \
   } else {                                                                                              \
-    go(sumsq_tiles_kernel<G, false, true, MAXR, 0>);                                                    \
+    go(sumsq_tiles_kernel<G, false, true, MAXR, 0, kGeneral>);                                          \
   }
   if (from_g32) {
     if constexpr (MAXR != kSmallRanks) return SS_ERR_INVALID_ARG;
-    else if (vec) go(sumsq_tiles_kernel<SS_BF16, true, true, MAXR, 0>);
+    else if (vec) go(sumsq_tiles_kernel<SS_BF16, true, true, MAXR, 0, kGeneral>);
     else go(sumsq_tiles_kernel<SS_BF16, true, false, MAXR, 0>);
   } else if (vec && gt == SS_BF16) {
     SS_SUMSQ_RANKED(SS_BF16)
@@ -349,6 +404,13 @@ ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype 
 #undef SS_SUMSQ_NR
   if (launched != SS_OK) return launched;
   return launch_dependent(sum_slots_kernel, dim3(1), dim3(kSlotThreads), 0, stream, a.partials, a.ntiles + 1, out);
+}
+
+template <int MAXR>
+ss_status run_sumsq(const SumsqArgs<MAXR>& a, bool vec, bool shift_gout, bool from_g32, ss_dtype gt, double* out,
+                    void* stream) {
+  return shift_gout ? run_sumsq_t<MAXR, true>(a, vec, from_g32, gt, out, stream)
+                    : run_sumsq_t<MAXR, false>(a, vec, from_g32, gt, out, stream);
 }
 
 // Shared by ss_grad_sumsq and any entry point that supplies its own slots.
@@ -384,14 +446,16 @@ ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_g
   if (any_output_overlap(ranges)) return SS_ERR_OVERLAP;
   int h = common_phase(p16, p32);
   bool vec = h >= 0 && h < n;
+  bool shift_gout = false;
   if (!vec && g_out) {
     // the inputs at one phase and g_out at another: the groups follow the inputs (16-byte
-    // loads) and g_out is written element by element (it was the last array listed)
+    // loads) and g_out's values are realigned between lanes (it was the last array listed)
     const std::vector<uintptr_t> in32(p32.begin(), p32.end() - 1);
     const int hin = common_phase(p16, in32);
     if (hin >= 0 && hin < n) {
       h = hin;
       vec = true;
+      shift_gout = true;
     }
   }
   const int64_t head = vec ? h : 0;
@@ -415,12 +479,12 @@ ss_status grad_sumsq_impl(int64_t n, const float* g32, const void* const* rank_g
     SumsqArgs<kSmallRanks> a;
     std::memset(&a, 0, sizeof a);
     fill(a);
-    return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+    return run_sumsq(a, vec, shift_gout, from_g32, gt, sumsq_out, stream);
   }
   SumsqArgs<kLargeRanks> a;
   std::memset(&a, 0, sizeof a);
   fill(a);
-  return run_sumsq(a, vec, from_g32, gt, sumsq_out, stream);
+  return run_sumsq(a, vec, shift_gout, from_g32, gt, sumsq_out, stream);
 }
 
 }  // namespace

@@ -82,24 +82,27 @@ def test_sumsq_several_tiles_per_block(ss, N):
     assert again.item() == out.item()
 
 
-@pytest.mark.parametrize("N", [2, 8])
+@pytest.mark.parametrize("N", [2, 8, 64])
 @pytest.mark.parametrize("n", [1001, (1 << 20) + 7])
-def test_sumsq_gout_off_the_inputs_phase(ss, N, n):
-    """The rank gradients aligned and g_out one element off: the groups follow the gradients
-    (16-byte loads) and g_out is written element by element. g_out bit-exact, the sum within the
-    header's 5e-7 of the oracle's and the same bits on a second call."""
+@pytest.mark.parametrize("off", [1, 2, 3])
+def test_sumsq_gout_off_the_inputs_phase(ss, N, n, off):
+    """The rank gradients aligned and g_out `off` floats off their 16-byte phase: the groups follow
+    the gradients (16-byte loads) and g_out is written as aligned vectors realigned by shuffles
+    between neighbouring lanes (with the warps' edge elements one by one), for the per-rank-count
+    tiles (2, 8 ranks) and the general ones (64). g_out bit-exact and nothing written outside it,
+    the sum within the header's 5e-7 of the oracle's and the same bits on a second call."""
     import torch
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 8) for r in range(N)]
     G = [dev_bits(s, n) for s in specs]
-    base = torch.zeros(n + 1, dtype=torch.float32, device="cuda")
-    g_out = base[1:]
+    base = torch.zeros(n + off + 4, dtype=torch.float32, device="cuda")
+    g_out = base[off:off + n]
     out = torch.zeros(2, dtype=torch.float64, device="cuda")
     ws = workspace(ss, n)
     ss.ss_grad_sumsq(n, out[0:1], ws, rank_grads=G, post_scale=0.5, g_out=g_out)
     ss.ss_grad_sumsq(n, out[1:2], ws, rank_grads=G, post_scale=0.5, g_out=g_out)
     g = oracle.grad_reduce([synth.host_range(s, 0, n) for s in specs], oracle.BF16, post_scale=0.5)
     assert np.array_equal(g_out.cpu().numpy().view(np.uint32), g.view(np.uint32))
-    assert base[0].item() == 0.0
+    assert (base[:off] == 0).all() and (base[off + n:] == 0).all()
     o = out.cpu().numpy()
     ref = oracle.sumsq(g)
     assert o[0] == o[1] and abs(o[0] - ref) <= 5e-7 * ref
