@@ -699,6 +699,20 @@ def run_suite(args, device) -> dict:
                                                                   param16=p16[:m7])), (2 * N + 26) * m7)
         out[key] = by_ranks
         del G
+    # the reduce with every rank's view one element off the output's phase, across rank counts
+    if want("grad_reduce_off_by_one_by_ranks"):
+        G = []
+        for r in range(16):
+            t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
+            synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+            G.append(t[1:n])
+        m1 = n - 1
+        by_ranks = {}
+        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16):
+            Gn = G[:N]
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_reduce(Gn, m1, g32[:m1])), (2 * N + 4) * m1)
+        out["grad_reduce_off_by_one_by_ranks"] = by_ranks
+        del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):
         G = []

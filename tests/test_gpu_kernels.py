@@ -92,12 +92,14 @@ def test_reduce_views_scale_accumulate_flag(ss, offsets):
     assert flag.item() == 1
 
 
-@pytest.mark.parametrize("N,n", [(1, 27), (1, 300_007), (2, 1001), (2, 300_007), (8, 27), (8, 300_007), (9, 1001),
-                                 (9, 300_007), (64, 1001), (64, 300_007), (1024, 27), (1024, 1001)])
+@pytest.mark.parametrize("N,n", [(1, 27), (1, 300_007), (2, 1001), (2, 300_007), (7, 300_007), (8, 27),
+                                 (8, 300_007), (9, 1001), (9, 300_007), (64, 1001), (64, 300_007), (1024, 27),
+                                 (1024, 1001)])
 def test_reduce_shifted_loads(ss, N, n):
     """Every rank's view 3 elements into its buffer, the output aligned: the warp-cooperative
-    shifted reduce (runs of 31 groups, ranks summed in batches of 8), accumulating with a post
-    scale, from a 1-group body (n = 27) up; bit-exact against the oracle, both rank tables."""
+    shifted reduce (runs of 31 groups; 7-8 ranks double-buffered, the others in batches of 8),
+    accumulating with a post scale, from a 1-group body (n = 27) up; bit-exact against the
+    oracle, both rank tables."""
     import torch
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 6) for r in range(N)]
     G = [dev_bits(s, n, offset=3) for s in specs]
@@ -111,13 +113,14 @@ def test_reduce_shifted_loads(ss, N, n):
     assert flag.item() == 0
 
 
+@pytest.mark.parametrize("N,warps_per_sm", [(8, 16), (4, 32)])
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, 5)])
-def test_reduce_shifted_run_boundaries(ss, k, d):
-    """The shifted reduce's grid passes over SMs x 32 warps runs of 31 groups; bodies of just a
-    whole number of passes, or one run more or less: bit-exact, so every run is taken once."""
+def test_reduce_shifted_run_boundaries(ss, N, warps_per_sm, k, d):
+    """The shifted reduce's grid passes over SMs x 16 warps (7-8 ranks, double-buffered) or
+    SMs x 32 warps (other rank counts) runs of 31 groups; bodies of just a whole number of passes,
+    or one run more or less: bit-exact, so every run is taken once."""
     import torch
-    N = 4
-    runs = k * _sms() * 32 + d
+    runs = k * _sms() * warps_per_sm + d
     n = (runs * 31 + 2) * 8 + 5
     specs = [synth.normal(1e-3, synth.FP16, synth.GRAD, r, 7) for r in range(N)]
     G = [dev_bits(s, n, offset=5) for s in specs]
