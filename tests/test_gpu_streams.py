@@ -100,14 +100,15 @@ def test_graph_capture_replays_the_clipped_step(ss):
 
 
 def test_graph_capture_replays_the_shifted_load_steps(ss):
-    """The shifted-load kernel forms -- 8 ranks one element off the state's phase (double-buffered,
-    one phase), 4 ranks at mixed phases (double-buffered, a shift per rank), 16 ranks off phase
-    (single-buffered) -- each take their runs from a counter in shared memory; captured once into a
-    CUDA graph and replayed 3 times, equal bit for bit to the same calls run eagerly 3 times."""
+    """The warp-cooperative shifted-load kernel forms -- 8 ranks one element off the state's phase
+    (double-buffered, 384-thread blocks), 4 ranks at mixed phases (a shift per rank), 16 ranks off
+    phase (double-buffered, 256-thread blocks), 20 ranks off phase (single-buffered) -- each take
+    their runs from a counter in shared memory; captured once into a CUDA graph and replayed 3
+    times, equal bit for bit to the same calls run eagerly 3 times."""
     import torch
     n = 1_000_003
     hp = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=2)
-    cases = [(8, lambda r: 1), (4, lambda r: (r % 7) + 1), (16, lambda r: 3)]
+    cases = [(8, lambda r: 1), (4, lambda r: (r % 7) + 1), (16, lambda r: 3), (20, lambda r: 5)]
     G = []
     for N, off in cases:
         views = []
