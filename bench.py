@@ -693,25 +693,32 @@ def run_suite(args, device) -> dict:
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
             G.append(t[offset(r):offset(r) + m7])
         by_ranks = {}
-        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 12, 16, 32, 64):
+        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12, 13, 14, 16, 32, 64):
             Gn = G[:N]
             by_ranks[str(N)] = entry(timed(lambda: ss.ss_adam_step(hp, m7, *(t[:m7] for t in st), rank_grads=Gn,
                                                                   param16=p16[:m7])), (2 * N + 26) * m7)
         out[key] = by_ranks
         del G
     # the reduce with every rank's view one element off the output's phase, across rank counts
-    if want("grad_reduce_off_by_one_by_ranks"):
+    # (also accumulating into the output, and with rank r's view (r % 7) + 1 elements off)
+    for key, offset, acc, ranks in (
+            ("grad_reduce_off_by_one_by_ranks", lambda r: 1, False, (1, 2, 3, 4, 5, 6, 7, 8, 9, 16)),
+            ("grad_reduce_accumulate_off_by_one_by_ranks", lambda r: 1, True, (1, 2, 3, 4, 6, 8, 16)),
+            ("grad_reduce_mixed_phase_by_ranks", lambda r: (r % 7) + 1, False, (2, 3, 4, 6, 8, 12, 16, 64))):
+        if not want(key):
+            continue
+        m7 = n - 7
         G = []
-        for r in range(16):
+        for r in range(max(ranks)):
             t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
-            G.append(t[1:n])
-        m1 = n - 1
+            G.append(t[offset(r):offset(r) + m7])
         by_ranks = {}
-        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16):
+        for N in ranks:
             Gn = G[:N]
-            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_reduce(Gn, m1, g32[:m1])), (2 * N + 4) * m1)
-        out["grad_reduce_off_by_one_by_ranks"] = by_ranks
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_reduce(Gn, m7, g32[:m7], accumulate=acc)),
+                                     (2 * N + 4 + 4 * acc) * m7)
+        out[key] = by_ranks
         del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):

@@ -256,6 +256,34 @@ __device__ __forceinline__ void shift_down8(float (&g)[8], int sh) {
   }
 }
 
+// The 16-bit values SH .. SH + 7 of the 16 in (this lane's chunk c, the next
+// lane's chunk), still packed: only the ceil(SH / 2) words that hold values
+// from the next lane are shuffled, then funnel-shifted into place (all lanes of
+// the warp call it with the same SH). Shifting before widening moves half the
+// words a shift of the eight fp32 values would.
+template <int SH>
+__device__ __forceinline__ uint4 shift_chunk(const uint4& c) {
+  constexpr int nw = (SH + 1) / 2;
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t d[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < nw; ++j) d[j] = __shfl_down_sync(0xFFFFFFFFu, w[j], 1);
+  return window16<2 * SH>(c, make_uint4(d[0], d[1], d[2], d[3]));
+}
+
+__device__ __forceinline__ uint4 shift_chunk(const uint4& c, int sh) {
+  switch (sh) {  // warp-uniform
+    case 0: return c;
+    case 1: return shift_chunk<1>(c);
+    case 2: return shift_chunk<2>(c);
+    case 3: return shift_chunk<3>(c);
+    case 4: return shift_chunk<4>(c);
+    case 5: return shift_chunk<5>(c);
+    case 6: return shift_chunk<6>(c);
+    default: return shift_chunk<7>(c);
+  }
+}
+
 // ------------------------------------------------------------------ work division
 //
 // The step and reduce kernels run one wave of blocks, one per SM. A chunk is 32

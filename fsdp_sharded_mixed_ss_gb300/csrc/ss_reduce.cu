@@ -2,8 +2,10 @@
 // the fp32 rank-ordered sum of the ranks' 16-bit gradient shards, optionally
 // scaled, accumulated into the output and checked for non-finite values. Three
 // forms: 16-byte vectors when the ranks and the output share a 16-byte phase,
-// warp-cooperative shifted loads when the ranks share a phase that is not the
-// output's, element-wise otherwise.
+// warp-cooperative shifted loads when the output has a phase the ranks do not
+// share (at one phase or each at its own), element-wise otherwise (an output
+// that is not 16-byte aligned after any whole number of elements, or fewer than
+// three 8-element groups).
 #include "ss_common.cuh"
 
 namespace ss {
@@ -95,73 +97,61 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
   }
 }
 
-// Rank gradients all at one 16-byte phase that is not the fp32 output's (views
-// at an offset that is not a multiple of 8 elements into per-rank buffers,
-// with the output allocated per shard): warp-cooperative runs of kRun groups
-// (ss_common.cuh), the ranks' chunks loaded in batches of 8 and summed in rank
-// order before the shift, so each gradient byte is loaded once; the output
-// (and its old value when accumulating) stays in aligned 16-byte vectors.
-// Groups 0 and nvec - 1 and the head/tail elements go one by one.
+// Rank gradients off the fp32 output's 16-byte phase (views at an offset that
+// is not a multiple of 8 elements into per-rank buffers, with the output
+// allocated per shard): warp-cooperative runs of kRun groups (ss_common.cuh).
+// Ranks at one phase: their chunks are summed in rank order, then shifted once;
+// ranks at mixed phases: each rank's packed chunk is moved into place by its
+// own phase before it is added -- the same fp32 additions in the same order
+// either way. Each gradient byte is loaded once; the output (and its old value
+// when accumulating) stays in aligned 16-byte vectors. Groups 0 and nvec - 1
+// and the head/tail elements go one by one.
+//
+// The forms differ in how they keep enough bytes in flight:
+//  * 1-2 ranks: a warp takes U adjacent runs at a time and issues all their
+//    loads before the first is summed (one 1024-thread block per SM). With one
+//    run at a time the loads in flight per SM were too few: measured on GB300 at
+//    2^26 elements, one element off, 1 rank 0.67 of the copy peak -> 0.81 with
+//    U = 4 (0.76 with U = 8: fewer, larger batches end less evenly), 2 ranks
+//    0.80 -> 0.89 with U = 2 (0.83 with U = 4); 3-4 ranks measured slower this
+//    way (0.87 against 0.91-0.97) and take the any-rank form.
+//  * 7-8 ranks at one phase: register double-buffered (the next run's loads
+//    issued before the current run is summed and stored), one 512-thread block
+//    per SM. At mixed phases 8 ranks measured 0.87 there, so they take the
+//    any-rank form.
+//  * otherwise: batches of rank chunks, all loads of a batch before its adds,
+//    the old output values requested with the first batch; one 1024-thread
+//    block per SM.
 template <int MAXR>
 struct ShiftReduceArgs {
   ReduceArgs<MAXR> s;
-  int32_t rphase;  // byte offset of the ranks' group starts past a 16-byte boundary (even, nonzero)
+  uint8_t rphase[MAXR];  // byte offset of each rank's group starts past a 16-byte boundary (even)
 };
 
-template <int GT, int MAXR>
-__global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_kernel(const __grid_constant__ ShiftReduceArgs<MAXR> x) {
-  __shared__ unsigned next_run;
-  if (threadIdx.x == 0) next_run = 0;
-  __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  const ReduceArgs<MAXR>& a = x.s;
-  const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
-  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
-  const int sh = x.rphase >> 1;
-  const int lane = threadIdx.x & 31;
-  const ChunkMap<kReduceChunkThreads / 32> map(runs * 32);  // one "chunk" per run
-  bool bad = false;
-  for (int64_t run = map.take<false>(&next_run, lane); run < runs; run = map.take<false>(&next_run, lane)) {
-    const int64_t gi = 1 + run * kRun + lane;
-    const int64_t gl = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the arrays, unused
-    const int64_t el = a.head + gl * kGroup;
-    float g[8];
-    for (int r0 = 0; r0 < a.n_ranks; r0 += 8) {
-      uint4 w[8];
+// Scale, old value (accumulating), finiteness check and store of one body group's sums.
+template <int MAXR>
+__device__ __forceinline__ void reduce_store8(const ReduceArgs<MAXR>& a, int64_t e, float (&g)[8],
+                                              const float4 (&o)[2], bool acc, bool& bad) {
+  if (a.post_scale != 1.0f) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (r0 + j < a.n_ranks)
-          w[j] = __ldcs(reinterpret_cast<const uint4*>(
-              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) - x.rphase));
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (r0 + j < a.n_ranks) {
-          if (r0 + j == 0) widen8<GT>(w[j], g);
-          else add8<GT>(w[j], g);
-        }
-      }
-    }
-    shift_down8(g, sh);
-    if (lane < kRun && gi < nvec - 1) {
-      const int64_t e = a.head + gi * kGroup;
-      if (a.post_scale != 1.0f) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
-      }
-      if (a.accumulate) {
-        float o[8];
-        ld8f(a.out + e, o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = o[j] + g[j];
-      }
-      if (a.nonfinite) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-      }
-      st8f(a.out + e, g);
-    }
+    for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
   }
+  if (acc) {
+    const float ov[8] = {o[0].x, o[0].y, o[0].z, o[0].w, o[1].x, o[1].y, o[1].z, o[1].w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) g[j] = ov[j] + g[j];
+  }
+  if (a.nonfinite) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
+  }
+  st8f(a.out + e, g);
+}
+
+// The groups outside the body [1, nvec - 1) and the head/tail elements, one per
+// thread, then the block's non-finite flag (all threads call it).
+template <int GT, int MAXR>
+__device__ __forceinline__ void reduce_shift_edges(const ReduceArgs<MAXR>& a, int64_t nvec, int lane, bool bad) {
   const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int64_t lo_end = a.head + kGroup, hi_start = a.head + (nvec - 1) * kGroup;
   const int64_t n_edge = lo_end + (a.n - hi_start);
@@ -172,22 +162,17 @@ __global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_kernel(const
   }
 }
 
-// The same for 7 and 8 ranks, register double-buffered: the loads of a warp's
-// next run (the ranks' chunks, and the output's old values when accumulating)
-// are issued before the current run is summed and stored. One 512-thread block
-// per SM. Measured on GB300 at 2^26 elements with the views one element off:
-// 7 ranks 6697 GB/s against 6617 single-buffered, 8 ranks 6815 against 6451;
-// with fewer ranks the single-buffered form's 1024-thread blocks were faster
-// (1-6 ranks 4502-6815 against 4133-6467).
+// One run's loads of one lane: the ranks' aligned 16-byte chunks and, when
+// accumulating, its group's old output values.
 template <int NR>
 struct ShiftReduceGroup {
   uint4 r[NR];
-  float4 o[2];  // the output's old values (accumulating only)
+  float4 o[2];
 };
 
-template <int GT, int MAXR, int NR>
+template <int GT, int MAXR, int NR, bool MIXED>
 __device__ __forceinline__ void reduce_shift_load(const ShiftReduceArgs<MAXR>& x, int64_t run, int lane, int64_t nvec,
-                                                  ShiftReduceGroup<NR>& G) {
+                                                  bool acc, ShiftReduceGroup<NR>& G) {
   const ReduceArgs<MAXR>& a = x.s;
   const int64_t gi = 1 + run * kRun + lane;
   const int64_t gl = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the arrays, unused
@@ -195,17 +180,111 @@ __device__ __forceinline__ void reduce_shift_load(const ShiftReduceArgs<MAXR>& x
 #pragma unroll
   for (int r = 0; r < NR; ++r)
     G.r[r] = __ldcs(reinterpret_cast<const uint4*>(
-        reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r]) + el) - x.rphase));
-  if (a.accumulate && lane < kRun) {
+        reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r]) + el) - x.rphase[MIXED ? r : 0]));
+  if (acc && lane < kRun) {
     const int64_t gb = gi < nvec - 2 ? gi : nvec - 2;  // a body group's old values
     G.o[0] = __ldcs(reinterpret_cast<const float4*>(a.out + a.head + gb * kGroup));
     G.o[1] = __ldcs(reinterpret_cast<const float4*>(a.out + a.head + gb * kGroup) + 1);
   }
 }
 
-template <int GT, int MAXR, int NR>
+// Sums one run's chunks in rank order, moves the sums into place and stores the lane's body group.
+template <int GT, int MAXR, int NR, bool MIXED>
+__device__ __forceinline__ void reduce_shift_group(const ShiftReduceArgs<MAXR>& x, const ShiftReduceGroup<NR>& G,
+                                                   int64_t run, int lane, int64_t nvec, bool acc, bool& bad) {
+  float g[8];
+  if constexpr (MIXED) {
+    widen8<GT>(shift_chunk(G.r[0], x.rphase[0] >> 1), g);
+#pragma unroll
+    for (int r = 1; r < NR; ++r) add8<GT>(shift_chunk(G.r[r], x.rphase[r] >> 1), g);
+  } else {
+    widen8<GT>(G.r[0], g);
+#pragma unroll
+    for (int r = 1; r < NR; ++r) add8<GT>(G.r[r], g);
+    shift_down8(g, x.rphase[0] >> 1);
+  }
+  const int64_t gi = 1 + run * kRun + lane;
+  if (lane < kRun && gi < nvec - 1) reduce_store8(x.s, x.s.head + gi * kGroup, g, G.o, acc, bad);
+}
+
+// Runs a warp takes at a time in the 1-4-rank form: enough loads in flight per
+// SM without spilling in a 1024-thread block (64 registers a thread).
+#ifndef SS_RED_BATCH_MAX_RANKS
+#define SS_RED_BATCH_MAX_RANKS 2
+#endif
+#ifndef SS_RED_BATCH_RUNS_1
+#define SS_RED_BATCH_RUNS_1 4
+#endif
+#ifndef SS_RED_BATCH_RUNS
+#define SS_RED_BATCH_RUNS 2
+#endif
+__host__ __device__ constexpr int reduce_batch_runs(int nr, bool acc) {
+  return acc ? (nr <= 2 ? 2 : 1) : (nr == 1 ? SS_RED_BATCH_RUNS_1 : SS_RED_BATCH_RUNS);
+}
+
+template <int GT, int MAXR, int NR, bool ACC, bool MIXED>
+__global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_batch_kernel(
+    const __grid_constant__ ShiftReduceArgs<MAXR> x) {
+  constexpr int U = reduce_batch_runs(NR, ACC);
+  __shared__ unsigned next_batch;
+  if (threadIdx.x == 0) next_batch = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvec = (x.s.n - x.s.head) / kGroup;  // >= 3 on this path
+  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
+  const int64_t batches = (runs + U - 1) / U;
+  const int lane = threadIdx.x & 31;
+  const ChunkMap<kReduceChunkThreads / 32> map(batches * 32);  // one "chunk" per U adjacent runs
+  bool bad = false;
+  for (int64_t b = map.take<false>(&next_batch, lane); b < batches; b = map.take<false>(&next_batch, lane)) {
+    ShiftReduceGroup<NR> G[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) reduce_shift_load<GT, MAXR, NR, MIXED>(x, b * U + u, lane, nvec, ACC, G[u]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) reduce_shift_group<GT, MAXR, NR, MIXED>(x, G[u], b * U + u, lane, nvec, ACC, bad);
+  }
+  reduce_shift_edges<GT>(x.s, nvec, lane, bad);
+}
+
+// 7 and 8 ranks. Measured on GB300 at 2^26 elements with the views one element
+// off: 7 ranks 6697 GB/s against 6617 in the any-rank form below, 8 ranks 6815
+// against 6451; with 5-6 ranks the any-rank form's 1024-thread blocks were faster.
+template <int GT, int MAXR, int NR, bool MIXED>
 __global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) reduce_shift_pipe_kernel(
     const __grid_constant__ ShiftReduceArgs<MAXR> x) {
+  __shared__ unsigned next_run;
+  if (threadIdx.x == 0) next_run = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvec = (x.s.n - x.s.head) / kGroup;  // >= 3 on this path
+  const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
+  const int lane = threadIdx.x & 31;
+  const ChunkMap<kChunkWarps> map(runs * 32);  // one "chunk" per run
+  const bool acc = x.s.accumulate;
+  bool bad = false;
+  ShiftReduceGroup<NR> cur, nxt;
+  int64_t run = map.take<false>(&next_run, lane);
+  if (run < runs) reduce_shift_load<GT, MAXR, NR, MIXED>(x, run, lane, nvec, acc, cur);
+  while (run < runs) {  // warp-uniform
+    const int64_t rn = map.take<false>(&next_run, lane);
+    if (rn < runs) reduce_shift_load<GT, MAXR, NR, MIXED>(x, rn, lane, nvec, acc, nxt);
+    reduce_shift_group<GT, MAXR, NR, MIXED>(x, cur, run, lane, nvec, acc, bad);
+    cur = nxt;
+    run = rn;
+  }
+  reduce_shift_edges<GT>(x.s, nvec, lane, bad);
+}
+
+// Any rank count. Accumulating, the old values' registers leave room for
+// batches of 6 rank chunks (8 spilled).
+#ifndef SS_RED_ACC_BATCH
+#define SS_RED_ACC_BATCH 6
+#endif
+template <int GT, int MAXR, bool ACC, bool MIXED>
+__global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_kernel(const __grid_constant__ ShiftReduceArgs<MAXR> x) {
+  constexpr int B = ACC ? SS_RED_ACC_BATCH : 8;
   __shared__ unsigned next_run;
   if (threadIdx.x == 0) next_run = 0;
   __syncthreads();
@@ -214,84 +293,103 @@ __global__ void __launch_bounds__(kChunkThreads, kChunkBlocksPerSm) reduce_shift
   const ReduceArgs<MAXR>& a = x.s;
   const int64_t nvec = (a.n - a.head) / kGroup;  // >= 3 on this path
   const int64_t runs = (nvec - 2 + kRun - 1) / kRun;
-  const int sh = x.rphase >> 1;
   const int lane = threadIdx.x & 31;
-  const ChunkMap<kChunkWarps> map(runs * 32);  // one "chunk" per run
+  const ChunkMap<kReduceChunkThreads / 32> map(runs * 32);  // one "chunk" per run
   bool bad = false;
-  ShiftReduceGroup<NR> cur, nxt;
-  int64_t run = map.take<false>(&next_run, lane);
-  if (run < runs) reduce_shift_load<GT>(x, run, lane, nvec, cur);
-  while (run < runs) {  // warp-uniform
-    const int64_t rn = map.take<false>(&next_run, lane);
-    if (rn < runs) reduce_shift_load<GT>(x, rn, lane, nvec, nxt);
-    float g[8];
-    widen8<GT>(cur.r[0], g);
-#pragma unroll
-    for (int r = 1; r < NR; ++r) add8<GT>(cur.r[r], g);
-    shift_down8(g, sh);
+  for (int64_t run = map.take<false>(&next_run, lane); run < runs; run = map.take<false>(&next_run, lane)) {
     const int64_t gi = 1 + run * kRun + lane;
-    if (lane < kRun && gi < nvec - 1) {
-      const int64_t e = a.head + gi * kGroup;
-      if (a.post_scale != 1.0f) {
+    const int64_t gl = gi < nvec - 1 ? gi : nvec - 1;  // past the body: a chunk inside the arrays, unused
+    const int64_t el = a.head + gl * kGroup;
+    const bool body = lane < kRun && gi < nvec - 1;
+    float g[8];
+    float4 o[2];
+    for (int r0 = 0; r0 < a.n_ranks; r0 += B) {
+      uint4 w[B];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
+      for (int j = 0; j < B; ++j)
+        if (r0 + j < a.n_ranks)
+          w[j] = __ldcs(reinterpret_cast<const uint4*>(
+              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) -
+              x.rphase[MIXED ? r0 + j : 0]));
+      if (ACC && r0 == 0 && body) {
+        o[0] = __ldcs(reinterpret_cast<const float4*>(a.out + a.head + gi * kGroup));
+        o[1] = __ldcs(reinterpret_cast<const float4*>(a.out + a.head + gi * kGroup) + 1);
       }
-      if (a.accumulate) {
-        const float o[8] = {cur.o[0].x, cur.o[0].y, cur.o[0].z, cur.o[0].w, cur.o[1].x, cur.o[1].y, cur.o[1].z, cur.o[1].w};
 #pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = o[j] + g[j];
+      for (int j = 0; j < B; ++j) {
+        if (r0 + j < a.n_ranks) {
+          const uint4 c = MIXED ? shift_chunk(w[j], x.rphase[r0 + j] >> 1) : w[j];
+          if (r0 + j == 0) widen8<GT>(c, g);
+          else add8<GT>(c, g);
+        }
       }
-      if (a.nonfinite) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) bad |= !finite(g[j]);
-      }
-      st8f(a.out + e, g);
     }
-    cur = nxt;
-    run = rn;
+    if constexpr (!MIXED) shift_down8(g, x.rphase[0] >> 1);
+    if (body) reduce_store8(a, a.head + gi * kGroup, g, o, ACC, bad);
   }
-  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int64_t lo_end = a.head + kGroup, hi_start = a.head + (nvec - 1) * kGroup;
-  const int64_t n_edge = lo_end + (a.n - hi_start);
-  if (tid < n_edge) reduce_one<GT>(a, tid < lo_end ? tid : hi_start + (tid - lo_end), bad);
-  if (a.nonfinite) {
-    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
-    if (any && lane == 0) *a.nonfinite = 1;
-  }
+  reduce_shift_edges<GT>(a, nvec, lane, bad);
 }
 
-template <int G, int MAXR, int NR>
+template <int G, int MAXR, int NR, bool MIXED>
+ss_status launch_reduce_shift_batch(const ShiftReduceArgs<MAXR>& x, int64_t runs, void* stream) {
+  auto go = [&](auto* fn, int u) {
+    const int64_t batches = (runs + u - 1) / u;
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), batches * 32, kReduceChunkThreads), x, stream,
+                  kReduceChunkThreads);
+  };
+  if (x.s.accumulate) return go(reduce_shift_batch_kernel<G, MAXR, NR, true, MIXED>, reduce_batch_runs(NR, true));
+  return go(reduce_shift_batch_kernel<G, MAXR, NR, false, MIXED>, reduce_batch_runs(NR, false));
+}
+
+template <int G, int MAXR, int NR, bool MIXED>
 ss_status launch_reduce_shift_pipe(const ShiftReduceArgs<MAXR>& x, int64_t runs, void* stream) {
-  auto* fn = reduce_shift_pipe_kernel<G, MAXR, NR>;
+  auto* fn = reduce_shift_pipe_kernel<G, MAXR, NR, MIXED>;
   return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kChunkThreads), x, stream, kChunkThreads);
 }
 
+template <int G, int MAXR, bool MIXED>
+ss_status launch_reduce_shift(const ShiftReduceArgs<MAXR>& x, void* stream) {
+  const ReduceArgs<MAXR>& a = x.s;
+  const int64_t runs = ((a.n - a.head) / kGroup - 2 + kRun - 1) / kRun;
+  if constexpr (MAXR == kSmallRanks) {
+    switch (a.n_ranks) {
+      case 1: return launch_reduce_shift_batch<G, MAXR, 1, MIXED>(x, runs, stream);
+      case 2:
+        if constexpr (SS_RED_BATCH_MAX_RANKS >= 2) return launch_reduce_shift_batch<G, MAXR, 2, MIXED>(x, runs, stream);
+        break;
+      case 3:
+        if constexpr (SS_RED_BATCH_MAX_RANKS >= 3) return launch_reduce_shift_batch<G, MAXR, 3, MIXED>(x, runs, stream);
+        break;
+      case 4:
+        if constexpr (SS_RED_BATCH_MAX_RANKS >= 4) return launch_reduce_shift_batch<G, MAXR, 4, MIXED>(x, runs, stream);
+        break;
+      case 7: if (!MIXED) return launch_reduce_shift_pipe<G, MAXR, 7, false>(x, runs, stream); break;
+      case 8: if (!MIXED) return launch_reduce_shift_pipe<G, MAXR, 8, false>(x, runs, stream); break;
+      default: break;
+    }
+  }
+  auto go = [&](auto* fn) {
+    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kReduceChunkThreads), x, stream,
+                  kReduceChunkThreads);
+  };
+  return a.accumulate ? go(reduce_shift_kernel<G, MAXR, true, MIXED>) : go(reduce_shift_kernel<G, MAXR, false, MIXED>);
+}
 
+// rphase: each rank's byte phase at the output's group starts (even; not all zero).
 template <int MAXR>
-ss_status run_reduce_shift(const ReduceArgs<MAXR>& a, int rphase, ss_dtype gt, void* stream) {
+ss_status run_reduce_shift(const ReduceArgs<MAXR>& a, const uint8_t* rphase, ss_dtype gt, void* stream) {
   ShiftReduceArgs<MAXR> x;
   std::memset(&x, 0, sizeof x);
   x.s = a;
-  x.rphase = rphase;
-  const int64_t runs = ((a.n - a.head) / kGroup - 2 + kRun - 1) / kRun;
-#define SS_REDP(G, R) \
-  case R: return launch_reduce_shift_pipe<G, MAXR, R>(x, runs, stream);
-#define SS_REDS_CASE(G)                                                                              \
-  if (gt == G) {                                                                                     \
-    if constexpr (MAXR == kSmallRanks) {                                                             \
-      switch (a.n_ranks) {                                                                           \
-        SS_REDP(G, 7) SS_REDP(G, 8)                                                                  \
-        default: break;                                                                              \
-      }                                                                                              \
-    }                                                                                                \
-    auto* fn = reduce_shift_kernel<G, MAXR>;                                                         \
-    return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kReduceChunkThreads), x, stream, \
-                  kReduceChunkThreads);                                                              \
+  bool mixed = false;
+  for (int32_t r = 0; r < a.n_ranks; ++r) {
+    x.rphase[r] = rphase[r];
+    mixed = mixed || rphase[r] != rphase[0];
   }
-  SS_REDS_CASE(SS_BF16)
-  SS_REDS_CASE(SS_FP16)
-#undef SS_REDS_CASE
-#undef SS_REDP
+  if (gt == SS_BF16) return mixed ? launch_reduce_shift<SS_BF16, MAXR, true>(x, stream)
+                                  : launch_reduce_shift<SS_BF16, MAXR, false>(x, stream);
+  if (gt == SS_FP16) return mixed ? launch_reduce_shift<SS_FP16, MAXR, true>(x, stream)
+                                  : launch_reduce_shift<SS_FP16, MAXR, false>(x, stream);
   return SS_ERR_DTYPE;
 }
 
@@ -346,12 +444,17 @@ ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtyp
   // the ranks at one phase, the output at another: groups aligned for the output, the
   // ranks read by the warp-cooperative shifted loads
   int64_t head = vec ? h : 0;
-  int rphase = 0;
-  if (!vec && common_phase(p16, {}) >= 0) {
+  bool shifted = false;
+  std::vector<uint8_t> rphase;
+  if (!vec) {
     const int h32 = common_phase({}, p32);
     if (h32 >= 0 && n - h32 >= 3 * kGroup) {
+      // every rank's byte phase at the output's group starts (not all zero: else vec)
+      shifted = true;
       head = h32;
-      rphase = static_cast<int>((reinterpret_cast<uintptr_t>(rank_grads[0]) + 2u * h32) & 15u);
+      rphase.resize(n_ranks);
+      for (int32_t r = 0; r < n_ranks; ++r)
+        rphase[r] = static_cast<uint8_t>((reinterpret_cast<uintptr_t>(rank_grads[r]) + 2u * h32) & 15u);
     }
   }
   auto fill = [&](auto& a) {
@@ -368,12 +471,12 @@ ss_status ss_grad_reduce(const void* const* rank_grads, int32_t n_ranks, ss_dtyp
     ReduceArgs<kSmallRanks> a;
     std::memset(&a, 0, sizeof a);
     fill(a);
-    return rphase ? run_reduce_shift(a, rphase, gdtype, stream) : run_reduce(a, vec, gdtype, stream);
+    return shifted ? run_reduce_shift(a, rphase.data(), gdtype, stream) : run_reduce(a, vec, gdtype, stream);
   }
   ReduceArgs<kLargeRanks> a;
   std::memset(&a, 0, sizeof a);
   fill(a);
-  return rphase ? run_reduce_shift(a, rphase, gdtype, stream) : run_reduce(a, vec, gdtype, stream);
+  return shifted ? run_reduce_shift(a, rphase.data(), gdtype, stream) : run_reduce(a, vec, gdtype, stream);
 }
 
 }  // extern "C"

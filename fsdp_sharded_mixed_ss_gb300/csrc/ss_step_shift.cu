@@ -1,12 +1,12 @@
 // ss_step_shift.cu -- the fused shard step (ss_adam_step) when 16-bit arrays are
 // off the fp32 state's 16-byte phase: gradient views at boundaries that are not
 // multiples of 8 elements, or param16 inside a flat buffer at such a boundary
-// (and, at phase 0, aligned gradients of 9-16 ranks, where the double-buffered
-// form here measured fastest). Three kernel forms share the per-element
-// arithmetic of ss_math.cuh: a warp-cooperative double-buffered one for up to
-// 16 ranks at one phase, or up to 8 with each rank shifted by its own phase; a
-// warp-cooperative single-buffered one for more ranks at one phase; and a
-// per-thread one for more ranks at mixed phases (or an fp32 gradient with
+// (and, at phase 0, aligned gradients of 4, 5 and 9-16 ranks, where the
+// double-buffered form here measured fastest). Three kernel forms share the
+// per-element arithmetic of ss_math.cuh: a warp-cooperative double-buffered one
+// for up to 16 ranks at one phase, or up to 12 with each rank shifted by its own
+// phase; a warp-cooperative single-buffered one for more ranks at one phase; and
+// a per-thread one for more ranks at mixed phases (or an fp32 gradient with
 // param16 off phase). Each gradient byte is loaded once in the
 // warp-cooperative forms.
 #include "ss_step.cuh"
@@ -58,8 +58,15 @@ __device__ __forceinline__ void st16_at_phase(void* p, const uint4& v, int phase
   }
 }
 
+// The per-thread form: at least 2 blocks of 256 threads per SM (128 registers). With the
+// state requested before the gradients it needs 138 and the occupancy halves: measured on
+// GB300 at 2^26 elements, 9-64 ranks at mixed phases 0.46-0.52 of the copy peak at one block
+// per SM against 0.74-0.82 at two.
+#ifndef SS_SHIFT_THREAD_BLOCKS
+#define SS_SHIFT_THREAD_BLOCKS 2
+#endif
 template <int GT, int PT, bool FROM_G32, bool WRITE_P16, int MAXR>
-__global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
+__global__ void __launch_bounds__(kThreads, SS_SHIFT_THREAD_BLOCKS) adam_shift_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
   pdl_wait();
   pdl_trigger();
   const StepArgs<MAXR>& a = x.s;
@@ -72,6 +79,12 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
   bool bad = false;
   for (int64_t gi = g_lo + tid; gi < g_hi; gi += stride) {
     const int64_t e = a.head + gi * kGroup;
+    // the group's state is requested first, so it arrives with the gradients (no output
+    // overlaps an input, so nothing stored below changes it)
+    float p[8], m[8], v[8];
+    ld8f(a.master + e, p);
+    ld8f(a.m + e, m);
+    ld8f(a.v + e, v);
     float g[8];
     if constexpr (FROM_G32) {
       ld8f(a.g32 + e, g);
@@ -112,10 +125,6 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
 #pragma unroll
       for (int j = 0; j < 8; ++j) g[j] = g[j] * gs;
     }
-    float p[8], m[8], v[8];
-    ld8f(a.master + e, p);
-    ld8f(a.m + e, m);
-    ld8f(a.v + e, v);
 #pragma unroll
     for (int j = 0; j < 8; ++j) adamw_elem(a.k, g[j], p[j], m[j], v[j]);
     st8f(a.master + e, p);
@@ -188,12 +197,15 @@ __global__ void __launch_bounds__(kThreads) adam_shift_kernel(const __grid_const
 #ifndef SS_SHIFT_PIPE_MAX_RANKS
 #define SS_SHIFT_PIPE_MAX_RANKS 16
 #endif
-// Up to this many ranks at mixed phases take the double-buffered warp-cooperative kernel
-// (measured on GB300 at 2^26 elements with 16 allowed: 9 ranks 0.82 of the copy peak against
-// 0.73 per-thread, but 12 and 16 ranks 0.67 and 0.62 against 0.77 and 0.81 -- there the
-// per-rank shifts cost more issue slots than the update itself).
+// Up to this many ranks at mixed phases take the double-buffered warp-cooperative kernel,
+// each rank's packed chunk shifted by its own phase. Measured on GB300 at 2^26 elements, rank
+// r's view (r % 7) + 1 elements off: 9-11 ranks 0.85-0.86 of the copy peak against 0.74-0.75
+// per-thread, 12 ranks 0.78 against 0.77, 13-16 ranks 0.66-0.78 against 0.78-0.81.
 #ifndef SS_SHIFT_MIXED_MAX_RANKS
-#define SS_SHIFT_MIXED_MAX_RANKS 8
+#define SS_SHIFT_MIXED_MAX_RANKS 12
+#endif
+#ifndef SS_SHIFT_MIXED_VEC
+#define SS_SHIFT_MIXED_VEC 0
 #endif
 template <int NR>
 struct ShiftShape {
@@ -333,17 +345,10 @@ __global__ void __launch_bounds__(ShiftShape<NR>::kThreadsPerBlock, ShiftShape<N
     }
     float g[8];
     if constexpr (MIXED) {
-      // each rank's values moved into place by its own phase, then added in rank order
-      widen8<GT>(cur.r[0], g);
-      shift_down8(g, x.rphase[0] >> 1);
+      // each rank's packed values moved into place by its own phase, then added in rank order
+      widen8<GT>(shift_chunk(cur.r[0], x.rphase[0] >> 1), g);
 #pragma unroll
-      for (int r = 1; r < NR; ++r) {
-        float t[8];
-        widen8<GT>(cur.r[r], t);
-        shift_down8(t, x.rphase[r] >> 1);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) g[j] = g[j] + t[j];
-      }
+      for (int r = 1; r < NR; ++r) add8<GT>(shift_chunk(cur.r[r], x.rphase[r] >> 1), g);
     } else {
       widen8<GT>(cur.r[0], g);
 #pragma unroll
@@ -376,7 +381,7 @@ __global__ void __launch_bounds__(ShiftShape<NR>::kThreadsPerBlock, ShiftShape<N
 constexpr int kShiftVecBatch = SS_SHIFT_VEC_BATCH;
 constexpr int kShiftVecThreads = SS_SHIFT_VEC_THREADS;
 
-template <int GT, int PT, bool WRITE_P16, int MAXR>
+template <int GT, int PT, bool WRITE_P16, bool MIXED, int MAXR>
 __global__ void __launch_bounds__(kShiftVecThreads, 1)
     adam_shift_vec_kernel(const __grid_constant__ ShiftArgs<MAXR> x) {
   __shared__ unsigned next_run;
@@ -413,7 +418,8 @@ __global__ void __launch_bounds__(kShiftVecThreads, 1)
       for (int j = 0; j < kShiftVecBatch; ++j)
         if (r0 + j < a.n_ranks)
           w[j] = __ldcs(reinterpret_cast<const uint4*>(
-              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) - x.rphase[0]));
+              reinterpret_cast<const char*>(static_cast<const uint16_t*>(a.ranks.p[r0 + j]) + el) -
+              x.rphase[MIXED ? r0 + j : 0]));
       if (r0 == 0 && body) {
         s4[0] = __ldcs(reinterpret_cast<const float4*>(a.master + e));
         s4[1] = __ldcs(reinterpret_cast<const float4*>(a.master + e) + 1);
@@ -425,12 +431,14 @@ __global__ void __launch_bounds__(kShiftVecThreads, 1)
 #pragma unroll
       for (int j = 0; j < kShiftVecBatch; ++j) {
         if (r0 + j < a.n_ranks) {
-          if (r0 + j == 0) widen8<GT>(w[j], g);
-          else add8<GT>(w[j], g);
+          // at mixed phases each rank's packed values are moved into place before they are added
+          const uint4 c = MIXED ? shift_chunk(w[j], x.rphase[r0 + j] >> 1) : w[j];
+          if (r0 + j == 0) widen8<GT>(c, g);
+          else add8<GT>(c, g);
         }
       }
     }
-    shift_down8(g, sh);
+    if constexpr (!MIXED) shift_down8(g, sh);
     if (body) {
       float p[8] = {s4[0].x, s4[0].y, s4[0].z, s4[0].w, s4[1].x, s4[1].y, s4[1].z, s4[1].w};
       float m[8] = {s4[2].x, s4[2].y, s4[2].z, s4[2].w, s4[3].x, s4[3].y, s4[3].z, s4[3].w};
@@ -456,9 +464,9 @@ ss_status launch_shift_pipe_n(const ShiftArgs<MAXR>& x, void* stream) {
   return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, threads), x, stream, threads);
 }
 
-template <int G, int P, bool W, int MAXR>
+template <int G, int P, bool W, bool MIXED, int MAXR>
 ss_status launch_shift_vec(const ShiftArgs<MAXR>& x, void* stream) {
-  auto* fn = adam_shift_vec_kernel<G, P, W, MAXR>;
+  auto* fn = adam_shift_vec_kernel<G, P, W, MIXED, MAXR>;
   const int64_t runs = ((x.s.n - x.s.head) / kGroup - 2 + kRun - 1) / kRun;
   return launch(fn, grid_for(reinterpret_cast<const void*>(fn), runs * 32, kShiftVecThreads), x, stream,
                 kShiftVecThreads);
@@ -467,33 +475,22 @@ ss_status launch_shift_vec(const ShiftArgs<MAXR>& x, void* stream) {
 template <int G, int P, bool W, bool MIXED, int MAXR>
 ss_status launch_shift_warp(const ShiftArgs<MAXR>& x, void* stream) {
   if constexpr (MAXR == kSmallRanks) {
+    constexpr int kMax = MIXED ? SS_SHIFT_MIXED_MAX_RANKS : SS_SHIFT_PIPE_MAX_RANKS;
+#define SS_SHIFT_PIPE_CASE(R) \
+  case R:                     \
+    if constexpr (R <= kMax) return launch_shift_pipe_n<G, P, W, MIXED, MAXR, R>(x, stream); \
+    break;
     switch (x.s.n_ranks) {
-      case 1: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 1>(x, stream);
-      case 2: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 2>(x, stream);
-      case 3: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 3>(x, stream);
-      case 4: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 4>(x, stream);
-      case 5: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 5>(x, stream);
-      case 6: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 6>(x, stream);
-      case 7: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 7>(x, stream);
-      case 8: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 8>(x, stream);
+      SS_SHIFT_PIPE_CASE(1) SS_SHIFT_PIPE_CASE(2) SS_SHIFT_PIPE_CASE(3) SS_SHIFT_PIPE_CASE(4)
+      SS_SHIFT_PIPE_CASE(5) SS_SHIFT_PIPE_CASE(6) SS_SHIFT_PIPE_CASE(7) SS_SHIFT_PIPE_CASE(8)
+      SS_SHIFT_PIPE_CASE(9) SS_SHIFT_PIPE_CASE(10) SS_SHIFT_PIPE_CASE(11) SS_SHIFT_PIPE_CASE(12)
+      SS_SHIFT_PIPE_CASE(13) SS_SHIFT_PIPE_CASE(14) SS_SHIFT_PIPE_CASE(15) SS_SHIFT_PIPE_CASE(16)
       default: break;
     }
-    if constexpr ((MIXED ? SS_SHIFT_MIXED_MAX_RANKS : SS_SHIFT_PIPE_MAX_RANKS) > 8) {
-      switch (x.s.n_ranks) {
-        case 9: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 9>(x, stream);
-        case 10: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 10>(x, stream);
-        case 11: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 11>(x, stream);
-        case 12: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 12>(x, stream);
-        case 13: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 13>(x, stream);
-        case 14: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 14>(x, stream);
-        case 15: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 15>(x, stream);
-        case 16: return launch_shift_pipe_n<G, P, W, MIXED, MAXR, 16>(x, stream);
-        default: break;
-      }
-    }
+#undef SS_SHIFT_PIPE_CASE
   }
-  if constexpr (MIXED) return SS_ERR_INVALID_ARG;  // not reached: mixed phases take the double-buffered form only
-  else return launch_shift_vec<G, P, W, MAXR>(x, stream);
+  if constexpr (MIXED && !SS_SHIFT_MIXED_VEC) return SS_ERR_INVALID_ARG;  // not reached: see launch_shift
+  else return launch_shift_vec<G, P, W, MIXED, MAXR>(x, stream);
 }
 
 template <int G, int P, bool F, bool W, int MAXR>
@@ -503,12 +500,13 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
   x.s = a;
   for (int32_t r = 0; r < a.n_ranks; ++r) x.rphase[r] = rphase[r];
   x.pphase = pphase;
-  // 16-bit gradients at one phase: the warp-cooperative forms (double-buffered up to 8
+  // 16-bit gradients at one phase: the warp-cooperative forms (double-buffered up to 16
   // ranks, single-buffered above), summing first and shifting once. At mixed phases, up
-  // to 8 ranks: the double-buffered form shifting each rank by its own phase (on GB300 at
-  // 2^26 elements 0.93-0.96 of the copy peak against 0.71-0.81 per-thread); more ranks:
-  // the per-thread form, which the per-rank shifts of the warp-cooperative one did not
-  // beat there (9-64 ranks: 0.72-0.82 either way)
+  // to 12 ranks: the double-buffered form shifting each rank's packed chunk by its own
+  // phase (on GB300 at 2^26 elements 1-8 ranks 0.92-0.98 of the copy peak against
+  // 0.71-0.81 per-thread); more ranks: the per-thread form, which the warp-cooperative
+  // single-buffered form with per-rank shifts did not beat there (13-64 ranks 0.75-0.83
+  // against 0.78-0.82)
   if constexpr (!F) {
     bool same = true;
     for (int32_t r = 1; r < a.n_ranks; ++r) same = same && rphase[r] == rphase[0];
@@ -516,6 +514,9 @@ ss_status launch_shift(const StepArgs<MAXR>& a, const uint8_t* rphase, uint8_t p
     if constexpr (MAXR == kSmallRanks) {
       if (a.n_ranks <= SS_SHIFT_MIXED_MAX_RANKS) return launch_shift_warp<G, P, W, true, MAXR>(x, stream);
     }
+#if SS_SHIFT_MIXED_VEC
+    return launch_shift_vec<G, P, W, true, MAXR>(x, stream);
+#endif
   }
   // more ranks at mixed phases, or an fp32 gradient with param16 off phase: the per-thread form
   auto* fn = adam_shift_kernel<G, P, F, W, MAXR>;

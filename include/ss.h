@@ -27,8 +27,12 @@
  *   - Layout: every array is dense (stride 1) in the order of the flat
  *     parameter vector. fp32 arrays must be 4-byte aligned, 16-bit arrays
  *     2-byte aligned (SS_ERR_ALIGN otherwise). The kernels use 16-byte vector
- *     accesses when all arrays of a call share one 16-byte phase and fall back
- *     to element accesses otherwise (same results, lower bandwidth).
+ *     accesses when all arrays of a call share one 16-byte phase; when the fp32
+ *     arrays share one but 16-bit arrays do not (views at offsets that are not
+ *     multiples of 8 elements), the 16-bit arrays are read as aligned 16-byte
+ *     chunks and realigned in registers; with no common fp32 phase the kernels
+ *     fall back to element accesses. The results are the same in every case;
+ *     only the bandwidth differs.
  */
 #ifndef SS_H
 #define SS_H

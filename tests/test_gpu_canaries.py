@@ -4,8 +4,8 @@ Each output (master, m, v, param16, g_out, the reduce output, the flat unit and 
 into a larger buffer whose elements before and after the view hold a canary bit pattern. The calls run
 on ragged lengths with views at offsets that select each kernel form -- aligned double-buffered,
 single-buffered, warp-cooperative shifted (one phase and mixed phases, 512-, 384- and 256-thread
-blocks), per-thread shifted, element-wise, the fp32-gradient form; the reduce's vector, shifted and
-element-wise forms; the sum of squares with g_out aligned, realigned between lanes and element by
+blocks), per-thread shifted, element-wise, the fp32-gradient form; the reduce's vector and shifted
+forms (one phase and mixed phases); the sum of squares with g_out aligned, realigned between lanes and element by
 element; the copies at and off the shards' phase -- and every canary must be intact afterwards, so no
 form writes outside its arrays (the head/tail and first/last-group edges included).
 """
@@ -69,7 +69,8 @@ STEP_FORMS = [  # (N, gradient view offset of rank r, master/m/v offsets, param1
     (12, lambda r: 0, (0, 0, 0), 0),             # aligned 9-16 ranks: warp-cooperative, 256-thread blocks
     (12, lambda r: 7, (0, 0, 0), 2),             # one phase off, 256-thread blocks
     (4, lambda r: (r % 7) + 1, (0, 0, 0), 0),    # mixed phases: a shift per rank
-    (12, lambda r: (r % 7) + 1, (0, 0, 0), 0),   # mixed phases, more ranks: per-thread
+    (12, lambda r: (r % 7) + 1, (0, 0, 0), 0),   # mixed phases, 256-thread blocks
+    (13, lambda r: (r % 7) + 1, (0, 0, 0), 3),   # mixed phases, more ranks: per-thread, param16 off too
     (20, lambda r: 1, (0, 0, 0), 0),             # one phase off, more ranks: single-buffered warp-cooperative
     (4, lambda r: 0, (1, 2, 0), 0),              # no common fp32 phase: element-wise
 ]
@@ -109,10 +110,15 @@ def test_step_from_fp32_gradient_writes_only_its_arrays(ss):
 REDUCE_FORMS = [  # (N, gradient view offset of rank r, output offset)
     (4, lambda r: 0, 0),             # vector, chunked
     (16, lambda r: 0, 0),            # vector, grid-stride
-    (2, lambda r: 1, 0),             # shifted, single-buffered
+    (1, lambda r: 1, 0),             # shifted, four runs a warp at a time
+    (3, lambda r: 2, 0),             # shifted, two runs at a time (one accumulating)
+    (6, lambda r: 1, 0),             # shifted, batches of rank chunks
     (8, lambda r: 5, 0),             # shifted, double-buffered
     (8, lambda r: 0, 3),             # the output off the ranks' phase
-    (4, lambda r: (r % 7) + 1, 0),   # mixed phases: element-wise
+    (4, lambda r: (r % 7) + 1, 0),   # mixed phases, two runs at a time
+    (8, lambda r: (r % 7) + 1, 0),   # mixed phases, double-buffered
+    (12, lambda r: (r % 7) + 1, 0),  # mixed phases, batches of rank chunks
+    (4, lambda r: (r % 7) + 1, 1),   # mixed phases, the output one float past a boundary (3 head elements)
 ]
 
 

@@ -92,13 +92,15 @@ def test_reduce_views_scale_accumulate_flag(ss, offsets):
     assert flag.item() == 1
 
 
-@pytest.mark.parametrize("N,n", [(1, 27), (1, 300_007), (2, 1001), (2, 300_007), (7, 300_007), (8, 27),
-                                 (8, 300_007), (9, 1001), (9, 300_007), (64, 1001), (64, 300_007), (1024, 27),
-                                 (1024, 1001)])
-def test_reduce_shifted_loads(ss, N, n):
+@pytest.mark.parametrize("N,n", [(1, 27), (1, 300_007), (2, 1001), (2, 300_007), (3, 300_007), (4, 1001),
+                                 (4, 300_007), (5, 300_007), (7, 300_007), (8, 27), (8, 300_007), (9, 1001),
+                                 (9, 300_007), (64, 1001), (64, 300_007), (1024, 27), (1024, 1001)])
+@pytest.mark.parametrize("accumulate", [True, False])
+def test_reduce_shifted_loads(ss, N, n, accumulate):
     """Every rank's view 3 elements into its buffer, the output aligned: the warp-cooperative
-    shifted reduce (runs of 31 groups; 7-8 ranks double-buffered, the others in batches of 8),
-    accumulating with a post scale, from a 1-group body (n = 27) up; bit-exact against the
+    shifted reduce (runs of 31 groups; 1-4 ranks several runs a warp at a time, 7-8 ranks
+    double-buffered, the others in batches of rank chunks), with a post scale, accumulating or
+    not (separate kernel instances), from a 1-group body (n = 27) up; bit-exact against the
     oracle, both rank tables."""
     import torch
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 6) for r in range(N)]
@@ -106,27 +108,60 @@ def test_reduce_shifted_loads(ss, N, n):
     init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
     out = init.clone()
     flag = torch.zeros(1, dtype=torch.int32, device="cuda")
-    ss.ss_grad_reduce(G, n, out, post_scale=0.5, accumulate=True, nonfinite_flag=flag)
-    acc = bits_of(init).copy()
-    oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, post_scale=0.5, accumulate_into=acc)
-    assert np.array_equal(out.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+    ss.ss_grad_reduce(G, n, out, post_scale=0.5, accumulate=accumulate, nonfinite_flag=flag)
+    acc = bits_of(init).copy() if accumulate else None
+    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, post_scale=0.5, accumulate_into=acc)
+    ref = acc if accumulate else ref
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
     assert flag.item() == 0
 
 
-@pytest.mark.parametrize("N,warps_per_sm", [(8, 16), (4, 32)])
-@pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, 5)])
-def test_reduce_shifted_run_boundaries(ss, N, warps_per_sm, k, d):
-    """The shifted reduce's grid passes over SMs x 16 warps (7-8 ranks, double-buffered) or
-    SMs x 32 warps (other rank counts) runs of 31 groups; bodies of just a whole number of passes,
-    or one run more or less: bit-exact, so every run is taken once."""
+@pytest.mark.parametrize("N", [2, 3, 4, 5, 7, 8, 9, 16, 64, 65])
+@pytest.mark.parametrize("n", [1001, 300_007])
+@pytest.mark.parametrize("accumulate", [True, False])
+def test_reduce_mixed_phases(ss, N, n, accumulate):
+    """Rank r's view (r % 7) + 1 elements into its buffer (every rank at its own phase), the
+    output aligned: each rank's packed chunk moved into place by its own phase before the
+    rank-ordered fp32 add, in every form (several runs at a time for 2-4 ranks, double-buffered
+    for 7-8, batches of rank chunks otherwise; 65 ranks the large rank table); fp16, bit-exact
+    against the oracle, with the non-finite flag raised by one rank's infinity."""
     import torch
-    runs = k * _sms() * warps_per_sm + d
+    specs = [synth.uniform(6e-5, synth.FP16, synth.GRAD, r, 8) for r in range(N)]
+    G = [dev_bits(s, n, offset=(r % 7) + 1) for r, s in enumerate(specs)]
+    init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
+    out = init.clone()
+    flag = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ss.ss_grad_reduce(G, n, out, post_scale=0.25, accumulate=accumulate, nonfinite_flag=flag)
+    acc = bits_of(init).copy() if accumulate else None
+    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], synth.FP16, post_scale=0.25, accumulate_into=acc)
+    ref = acc if accumulate else ref
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    assert flag.item() == 0
+    G[N - 1][n // 3] = float("inf")
+    ss.ss_grad_reduce(G, n, out, nonfinite_flag=flag)
+    assert flag.item() == 1
+
+
+@pytest.mark.parametrize("N,accumulate,runs_per_sm", [(8, False, 16), (5, False, 32), (4, False, 64), (3, True, 32),
+                                                      (2, True, 64), (1, False, 128), (1, True, 64)])
+@pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (1, 1), (2, 5)])
+def test_reduce_shifted_run_boundaries(ss, N, accumulate, runs_per_sm, k, d):
+    """The shifted reduce's grid passes over SMs x 16 warps x 1 run (7-8 ranks, double-buffered),
+    SMs x 32 warps x U runs (1-4 ranks, U runs a warp at a time: U = 4 for one rank, else 2;
+    accumulating 2 up to 2 ranks, else 1) or SMs x 32 warps x 1 run (other rank counts), runs of 31
+    groups; bodies of just a whole number of passes, or one run more or less: bit-exact, so every
+    run is taken once."""
+    import torch
+    runs = k * _sms() * runs_per_sm + d
     n = (runs * 31 + 2) * 8 + 5
     specs = [synth.normal(1e-3, synth.FP16, synth.GRAD, r, 7) for r in range(N)]
     G = [dev_bits(s, n, offset=5) for s in specs]
-    out = torch.empty(n, dtype=torch.float32, device="cuda")
-    ss.ss_grad_reduce(G, n, out)
-    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], synth.FP16)
+    init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
+    out = init.clone()
+    ss.ss_grad_reduce(G, n, out, accumulate=accumulate)
+    acc = bits_of(init).copy() if accumulate else None
+    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], synth.FP16, accumulate_into=acc)
+    ref = acc if accumulate else ref
     assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
@@ -298,8 +333,10 @@ def test_step_from_fp32_grad_matches_fused(ss):
     (2, lambda r: 1),            # one phase off: warp-cooperative double-buffered, 512-thread blocks
     (8, lambda r: 3),            # one phase off: warp-cooperative double-buffered, 384-thread blocks
     (4, lambda r: (r % 7) + 1),  # mixed phases: warp-cooperative double-buffered, a shift per rank
-    (12, lambda r: 5),           # one phase off: warp-cooperative single-buffered
-    (12, lambda r: (r % 7) + 1), # mixed phases, more ranks: the per-thread kernel
+    (12, lambda r: 5),           # one phase off: warp-cooperative double-buffered, 256-thread blocks
+    (20, lambda r: 5),           # one phase off: warp-cooperative single-buffered
+    (12, lambda r: (r % 7) + 1), # mixed phases, 256-thread blocks, a shift per rank
+    (13, lambda r: (r % 7) + 1), # mixed phases, more ranks: the per-thread kernel
 ])
 def test_step_options(ss, N, offsets):
     """post_scale, g_out, the non-finite flag, the device gradient scale and the skip flag through
@@ -431,15 +468,15 @@ def test_step_split_calls_agree(ss):
     assert torch.equal(pa.view(torch.int16), pb.view(torch.int16))
 
 
-@pytest.mark.parametrize("N", [1, 2, 3, 5, 6, 7, 8, 9])
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 6, 7, 8, 9, 11, 12, 13])
 @pytest.mark.parametrize("n", [27, 40, 1000, 300_007])
 @pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
 @pytest.mark.parametrize("same", [True, False])
 def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
     """Rank views off the aligned state's phase: all at one offset (1..7) or rank r at (r % 7) + 1
     (mixed phases), from a 1-group body (n = 27) to many runs per warp: the warp-cooperative
-    double-buffered kernel up to 8 ranks (one sum shifted once, or each rank shifted by its own
-    phase), for 9 ranks the single-buffered one (one phase) or the per-thread one (mixed); equal
+    double-buffered kernel (one sum shifted once, up to 16 ranks, or each rank's packed chunk
+    shifted by its own phase, up to 12), for 13 ranks at mixed phases the per-thread one; equal
     to the aligned kernel bit for bit and to the oracle."""
     import torch
     hp = dict(HP, step=5)
@@ -458,10 +495,10 @@ def test_step_shifted_loads_each_rank_count(ss, N, n, fmt, same):
     _check(*b, pb, ref, fmt)
 
 
-@pytest.mark.parametrize("N", [3, 8, 16, 65, 1024])
+@pytest.mark.parametrize("N", [3, 8, 12, 16, 65, 1024])
 def test_step_mixed_phases(ss, N):
     """Rank r's gradient view r % 8 elements into its buffer (so some ranks sit on the state's
-    16-byte phase and the others at every other phase): up to 8 ranks the warp-cooperative
+    16-byte phase and the others at every other phase): up to 12 ranks the warp-cooperative
     double-buffered kernel shifts each rank by its own phase before adding it in rank order, more
     ranks take the per-thread kernel (both rank-table sizes); bit-equal to the aligned kernel and
     within the tolerance of the oracle."""
