@@ -699,9 +699,11 @@ def run_suite(args, device) -> dict:
                                                                   param16=p16[:m7])), (2 * N + 26) * m7)
         out[key] = by_ranks
         del G
-    # the reduce with every rank's view one element off the output's phase, across rank counts
-    # (also accumulating into the output, and with rank r's view (r % 7) + 1 elements off)
-    for key, offset, acc, ranks in (
+    # the reduce across rank counts: aligned, and with every rank's view one element off the output's
+    # phase (also accumulating into the output, and with rank r's view (r % 7) + 1 elements off)
+    for key, offset, accum, ranks in (
+            ("grad_reduce_by_ranks", lambda r: 0, False, (1, 2, 3, 4, 6, 8, 16)),
+            ("grad_reduce_accumulate_by_ranks", lambda r: 0, True, (1, 2, 3, 4, 8)),
             ("grad_reduce_off_by_one_by_ranks", lambda r: 1, False, (1, 2, 3, 4, 5, 6, 7, 8, 9, 16)),
             ("grad_reduce_accumulate_off_by_one_by_ranks", lambda r: 1, True, (1, 2, 3, 4, 6, 8, 16)),
             ("grad_reduce_mixed_phase_by_ranks", lambda r: (r % 7) + 1, False, (2, 3, 4, 6, 8, 12, 16, 64))):
@@ -716,9 +718,24 @@ def run_suite(args, device) -> dict:
         by_ranks = {}
         for N in ranks:
             Gn = G[:N]
-            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_reduce(Gn, m7, g32[:m7], accumulate=acc)),
-                                     (2 * N + 4 + 4 * acc) * m7)
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_reduce(Gn, m7, g32[:m7], accumulate=accum)),
+                                     (2 * N + 4 + 4 * accum) * m7)
         out[key] = by_ranks
+        del G
+    # the sum of squares writing g_out, every rank's view one element off g_out's phase
+    if want("grad_sumsq_gout_off_by_one_by_ranks"):
+        m7 = n - 7
+        G = []
+        for r in range(64):
+            t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
+            synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
+            G.append(t[1:1 + m7])
+        by_ranks = {}
+        for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 64):
+            Gn = G[:N]
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_sumsq(m7, acc, ws, rank_grads=Gn, g_out=g32[:m7])),
+                                     (2 * N + 4) * m7)
+        out["grad_sumsq_gout_off_by_one_by_ranks"] = by_ranks
         del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):

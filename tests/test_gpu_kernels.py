@@ -56,7 +56,7 @@ def bits_of(t):
 
 # ----------------------------------------------------------------------------- reduce
 
-@pytest.mark.parametrize("N", [1, 2, 3, 8, 64, 65, 1024])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8, 64, 65, 1024])
 @pytest.mark.parametrize("fmt", [synth.BF16, synth.FP16])
 def test_reduce_bit_exact(ss, N, fmt):
     import torch
@@ -289,22 +289,25 @@ def test_step_chunk_boundaries(ss, N, from_g32, k, d):
     _check(master, m, v, p16, ref, synth.BF16)
 
 
-@pytest.mark.parametrize("N", [1, 4, 8, 9])
+@pytest.mark.parametrize("N,accumulate,chunks_per_warp", [(1, True, 2), (1, False, 4), (2, True, 2), (2, False, 2),
+                                                          (4, True, 1), (8, True, 1), (9, True, 1)])
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (2, 257), (3, -4096)])
-def test_reduce_chunk_boundaries(ss, N, k, d):
-    """The reduce around whole passes of its grid (32 chunks of 256 elements per block, one block
-    per SM) for the chunked form (up to 8 ranks) and the grid-stride one (9), accumulating into
-    the output: bit-exact, so no element is added twice or missed."""
+def test_reduce_chunk_boundaries(ss, N, accumulate, chunks_per_warp, k, d):
+    """The aligned reduce around whole passes of its grid (one 1024-thread block per SM, 32 warps,
+    each taking chunks_per_warp chunks of 256 elements at a time: 1-2 ranks batch 2-4 chunks, up to 8
+    ranks one, 9 ranks grid-stride), accumulating into the output or not: bit-exact, so no element
+    is added twice or missed."""
     import torch
-    n = k * _sms() * 32 * 32 * 8 + d
+    n = k * _sms() * 32 * chunks_per_warp * 32 * 8 + d
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 4) for r in range(N)]
     G = [dev_bits(s, n) for s in specs]
     init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
     out = init.clone()
-    ss.ss_grad_reduce(G, n, out, accumulate=True)
-    acc = bits_of(init).copy()
-    oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, accumulate_into=acc)
-    assert np.array_equal(out.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+    ss.ss_grad_reduce(G, n, out, accumulate=accumulate)
+    acc = bits_of(init).copy() if accumulate else None
+    ref = oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, accumulate_into=acc)
+    ref = acc if accumulate else ref
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
 
 
 def test_step_from_fp32_grad_matches_fused(ss):
