@@ -83,6 +83,110 @@ __global__ void __launch_bounds__(CHUNKED ? kReduceChunkThreads : kThreads) redu
   }
 }
 
+// Few ranks, warp-contiguous accesses: lane i takes elements 4i..4i+3 and
+// 128+4i..128+4i+3 of its warp's 256-element chunk, so every 16-byte access of
+// a warp to the fp32 output (the store, and the old values' load when
+// accumulating) covers 512 contiguous bytes -- whole 32-byte sectors, where the
+// 8-element groups of reduce_vec_kernel leave each instruction half of every
+// sector it touches -- and every 8-byte gradient load reads 256. Measured on
+// GB300 at 2^26 elements against reduce_vec_kernel: 1 rank 0.84 -> 0.87 of the
+// copy peak; accumulating, 1 / 2 / 3 ranks 0.87 / 0.95 / 0.99 -> 0.93 / 1.01 /
+// 1.02; without accumulating 2 and 3 ranks measured slower (0.90 / 0.93 against
+// 0.95 / 1.01: the halved gradient loads), 4 ranks the same.
+#ifndef SS_RED_QUAD_RANKS
+#define SS_RED_QUAD_RANKS 1  // up to this many ranks, not accumulating
+#endif
+#ifndef SS_RED_QUAD_ACC_RANKS
+#define SS_RED_QUAD_ACC_RANKS 3  // up to this many ranks, accumulating
+#endif
+static_assert(SS_RED_QUAD_RANKS <= 4 && SS_RED_QUAD_ACC_RANKS <= 4, "quad forms exist for 1-4 ranks");
+template <int GT, int MAXR, int NR, bool ACC>
+__global__ void __launch_bounds__(kReduceChunkThreads) reduce_quad_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  __shared__ unsigned next_chunk;
+  if (threadIdx.x == 0) next_chunk = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int lane = threadIdx.x & 31;
+  const ChunkMap<kReduceChunkThreads / 32> map(nvec);
+  bool bad = false;
+  for (int64_t c = map.take<false>(&next_chunk, lane); c < map.nchunk; c = map.take<false>(&next_chunk, lane)) {
+    uint2 w[2][NR];
+    float4 o[2];
+    bool ok[2];
+    int64_t e[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      ok[h] = c * 32 + 16 * h + lane / 2 < nvec;  // the lane's quad h lies in group 16h + lane/2 of the chunk
+      e[h] = a.head + c * 32 * kGroup + 128 * h + 4 * lane;
+      if (ok[h]) {
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+          w[h][r] = __ldcs(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(a.ranks.p[r]) + e[h]));
+        if (ACC) o[h] = __ldcs(reinterpret_cast<const float4*>(a.out + e[h]));
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      if (!ok[h]) continue;
+      float2 lo = widen2<GT>(w[h][0].x), hi = widen2<GT>(w[h][0].y);
+      float g[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+      for (int r = 1; r < NR; ++r) {
+        lo = widen2<GT>(w[h][r].x);
+        hi = widen2<GT>(w[h][r].y);
+        g[0] = g[0] + lo.x; g[1] = g[1] + lo.y; g[2] = g[2] + hi.x; g[3] = g[3] + hi.y;
+      }
+      if (a.post_scale != 1.0f) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) g[j] = g[j] * a.post_scale;
+      }
+      if (ACC) {
+        g[0] = o[h].x + g[0]; g[1] = o[h].y + g[1]; g[2] = o[h].z + g[2]; g[3] = o[h].w + g[3];
+      }
+      if (a.nonfinite) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) bad |= !finite(g[j]);
+      }
+      __stcs(reinterpret_cast<float4*>(a.out + e[h]), make_float4(g[0], g[1], g[2], g[3]));
+    }
+  }
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) reduce_one<GT>(a, tid < a.head ? tid : tail0 + (tid - a.head), bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && lane == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int G, int MAXR, int NR, bool ACC>
+ss_status launch_reduce_quad(const ReduceArgs<MAXR>& a, void* stream) {
+  auto* fn = reduce_quad_kernel<G, MAXR, NR, ACC>;
+  return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kReduceChunkThreads), a,
+                stream, kReduceChunkThreads);
+}
+
+// The quad form for this call, if it takes one (16-byte vectors, the small rank table).
+template <int G, int MAXR>
+bool reduce_quad(const ReduceArgs<MAXR>& a, ss_status& st, void* stream) {
+  if constexpr (MAXR != kSmallRanks) {
+    return false;
+  } else {
+#define SS_RED_QUAD(R)                                                                                       \
+  if (a.n_ranks == R) {                                                                                      \
+    if constexpr (SS_RED_QUAD_ACC_RANKS >= R)                                                                \
+      if (a.accumulate) return st = launch_reduce_quad<G, MAXR, R, true>(a, stream), true;                   \
+    if constexpr (SS_RED_QUAD_RANKS >= R)                                                                    \
+      if (!a.accumulate) return st = launch_reduce_quad<G, MAXR, R, false>(a, stream), true;                 \
+  }
+    SS_RED_QUAD(1) SS_RED_QUAD(2) SS_RED_QUAD(3) SS_RED_QUAD(4)
+#undef SS_RED_QUAD
+    return false;
+  }
+}
+
 template <int GT, int MAXR>
 __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
   pdl_wait();
@@ -397,6 +501,8 @@ template <int MAXR>
 ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* stream) {
 #define SS_RED_CASE(G)                                                                     \
   if (gt == G) {                                                                           \
+    ss_status st = SS_OK;                                                                  \
+    if (vec && reduce_quad<G>(a, st, stream)) return st;                                   \
     if (vec && a.n_ranks <= kReduceChunkRanks) {                                           \
       auto* fn = reduce_vec_kernel<G, MAXR, true>;                                         \
       return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kReduceChunkThreads), \

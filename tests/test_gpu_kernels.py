@@ -289,16 +289,16 @@ def test_step_chunk_boundaries(ss, N, from_g32, k, d):
     _check(master, m, v, p16, ref, synth.BF16)
 
 
-@pytest.mark.parametrize("N,accumulate,chunks_per_warp", [(1, True, 2), (1, False, 4), (2, True, 2), (2, False, 2),
-                                                          (4, True, 1), (8, True, 1), (9, True, 1)])
+@pytest.mark.parametrize("N,accumulate", [(1, True), (1, False), (2, True), (2, False), (3, True), (4, True),
+                                          (8, True), (9, True)])
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (2, 257), (3, -4096)])
-def test_reduce_chunk_boundaries(ss, N, accumulate, chunks_per_warp, k, d):
-    """The aligned reduce around whole passes of its grid (one 1024-thread block per SM, 32 warps,
-    each taking chunks_per_warp chunks of 256 elements at a time: 1-2 ranks batch 2-4 chunks, up to 8
-    ranks one, 9 ranks grid-stride), accumulating into the output or not: bit-exact, so no element
-    is added twice or missed."""
+def test_reduce_chunk_boundaries(ss, N, accumulate, k, d):
+    """The aligned reduce around whole passes of its grid (one 1024-thread block per SM whose 32
+    warps take chunks of 256 elements: 8 elements a lane, or, for 1 rank and for 1-3 ranks
+    accumulating, 4 + 4 at lane stride; 9 ranks grid-stride), accumulating into the output or not:
+    bit-exact, so no element is added twice or missed."""
     import torch
-    n = k * _sms() * 32 * chunks_per_warp * 32 * 8 + d
+    n = k * _sms() * 32 * 32 * 8 + d
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 4) for r in range(N)]
     G = [dev_bits(s, n) for s in specs]
     init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
