@@ -213,12 +213,16 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
 //
 // The forms differ in how they keep enough bytes in flight:
 //  * 1-2 ranks: a warp takes U adjacent runs at a time and issues all their
-//    loads before the first is summed (one 1024-thread block per SM). With one
-//    run at a time the loads in flight per SM were too few: measured on GB300 at
-//    2^26 elements, one element off, 1 rank 0.67 of the copy peak -> 0.81 with
-//    U = 4 (0.76 with U = 8: fewer, larger batches end less evenly), 2 ranks
-//    0.80 -> 0.89 with U = 2 (0.83 with U = 4); 3-4 ranks measured slower this
-//    way (0.87 against 0.91-0.97) and take the any-rank form.
+//    loads before the first is summed (one 1024-thread block per SM), and
+//    stores the sums through shared memory as warp-contiguous vectors
+//    (tx_store_run). With one run at a time the loads in flight per SM were too
+//    few: measured on GB300 at 2^26 elements, one element off, 1 rank 0.67 of
+//    the copy peak -> 0.81 with U = 4 (0.76 with U = 8: fewer, larger batches
+//    end less evenly) -> 0.88-0.89 with the contiguous stores, 2 ranks 0.80 ->
+//    0.88 with U = 2 (0.83 with U = 4) -> 0.94; accumulating 0.87-0.88 ->
+//    0.92-0.93. 3-4 ranks measured slower this way (0.93 against 0.94-0.99; the
+//    contiguous stores in the any-rank form cost 3-5% there) and take the
+//    any-rank form.
 //  * 7-8 ranks at one phase: register double-buffered (the next run's loads
 //    issued before the current run is summed and stored), one 512-thread block
 //    per SM. At mixed phases 8 ranks measured 0.87 there, so they take the
@@ -311,6 +315,64 @@ __device__ __forceinline__ void reduce_shift_group(const ShiftReduceArgs<MAXR>& 
   if (lane < kRun && gi < nvec - 1) reduce_store8(x.s, x.s.head + gi * kGroup, g, G.o, acc, bad);
 }
 
+// Stores through shared memory: a run's sums pass through the warp's 64
+// float4 slots so that the warp stores (and, accumulating, loads) the output as
+// consecutive 16-byte vectors -- vector f of a run (f < 62) holds elements
+// 4f..4f+3 of its 31 groups, and each instruction covers 512 contiguous bytes,
+// where each lane storing its own group leaves every instruction half of each
+// 32-byte sector it touches. tx_load_old: the run's old output values in that
+// layout (accumulating); tx_store_run: scale, old value, check and store.
+template <int MAXR>
+__device__ __forceinline__ void tx_load_old(const ReduceArgs<MAXR>& a, int64_t run, int lane, int64_t nvec,
+                                            float4 (&ot)[2]) {
+  const int64_t e0 = a.head + (1 + run * kRun) * kGroup;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int f = lane + 32 * k;
+    if (f < 2 * kRun && 1 + run * kRun + f / 2 < nvec - 1) ot[k] = __ldcs(reinterpret_cast<const float4*>(a.out + e0 + 4 * f));
+  }
+}
+
+template <int MAXR>
+__device__ __forceinline__ void tx_store_run(const ReduceArgs<MAXR>& a, float4* t, const float (&g)[8], int64_t run,
+                                             int lane, int64_t nvec, bool acc, const float4 (&ot)[2], bool& bad) {
+  t[2 * lane] = make_float4(g[0], g[1], g[2], g[3]);
+  t[2 * lane + 1] = make_float4(g[4], g[5], g[6], g[7]);
+  __syncwarp();
+  const int64_t e0 = a.head + (1 + run * kRun) * kGroup;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int f = lane + 32 * k;
+    if (f < 2 * kRun && 1 + run * kRun + f / 2 < nvec - 1) {
+      float4 v = t[f];
+      if (a.post_scale != 1.0f) {
+        v.x = v.x * a.post_scale; v.y = v.y * a.post_scale; v.z = v.z * a.post_scale; v.w = v.w * a.post_scale;
+      }
+      if (acc) {
+        v.x = ot[k].x + v.x; v.y = ot[k].y + v.y; v.z = ot[k].z + v.z; v.w = ot[k].w + v.w;
+      }
+      if (a.nonfinite) bad |= !finite(v.x) || !finite(v.y) || !finite(v.z) || !finite(v.w);
+      __stcs(reinterpret_cast<float4*>(a.out + e0 + 4 * f), v);
+    }
+  }
+  __syncwarp();  // the slots are free for the warp's next run
+}
+
+// The rank-ordered sum of one run's chunks, moved into place (all lanes).
+template <int GT, int MAXR, int NR, bool MIXED>
+__device__ __forceinline__ void shift_sum(const ShiftReduceArgs<MAXR>& x, const uint4 (&r)[NR], float (&g)[8]) {
+  if constexpr (MIXED) {
+    widen8<GT>(shift_chunk(r[0], x.rphase[0] >> 1), g);
+#pragma unroll
+    for (int k = 1; k < NR; ++k) add8<GT>(shift_chunk(r[k], x.rphase[k] >> 1), g);
+  } else {
+    widen8<GT>(r[0], g);
+#pragma unroll
+    for (int k = 1; k < NR; ++k) add8<GT>(r[k], g);
+    shift_down8(g, x.rphase[0] >> 1);
+  }
+}
+
 // Runs a warp takes at a time in the 1-4-rank form: enough loads in flight per
 // SM without spilling in a 1024-thread block (64 registers a thread).
 #ifndef SS_RED_BATCH_MAX_RANKS
@@ -331,6 +393,7 @@ __global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_batch_kernel
     const __grid_constant__ ShiftReduceArgs<MAXR> x) {
   constexpr int U = reduce_batch_runs(NR, ACC);
   __shared__ unsigned next_batch;
+  __shared__ float4 tx[kReduceChunkThreads / 32][64];  // each warp's run of sums, for tx_store_run
   if (threadIdx.x == 0) next_batch = 0;
   __syncthreads();
   pdl_wait();
@@ -340,13 +403,22 @@ __global__ void __launch_bounds__(kReduceChunkThreads) reduce_shift_batch_kernel
   const int64_t batches = (runs + U - 1) / U;
   const int lane = threadIdx.x & 31;
   const ChunkMap<kReduceChunkThreads / 32> map(batches * 32);  // one "chunk" per U adjacent runs
+  float4* t = tx[threadIdx.x >> 5];
   bool bad = false;
   for (int64_t b = map.take<false>(&next_batch, lane); b < batches; b = map.take<false>(&next_batch, lane)) {
     ShiftReduceGroup<NR> G[U];
+    float4 ot[U][2];
 #pragma unroll
-    for (int u = 0; u < U; ++u) reduce_shift_load<GT, MAXR, NR, MIXED>(x, b * U + u, lane, nvec, ACC, G[u]);
+    for (int u = 0; u < U; ++u) {
+      reduce_shift_load<GT, MAXR, NR, MIXED>(x, b * U + u, lane, nvec, false, G[u]);
+      if (ACC) tx_load_old(x.s, b * U + u, lane, nvec, ot[u]);
+    }
 #pragma unroll
-    for (int u = 0; u < U; ++u) reduce_shift_group<GT, MAXR, NR, MIXED>(x, G[u], b * U + u, lane, nvec, ACC, bad);
+    for (int u = 0; u < U; ++u) {
+      float g[8];
+      shift_sum<GT, MAXR, NR, MIXED>(x, G[u].r, g);
+      tx_store_run(x.s, t, g, b * U + u, lane, nvec, ACC, ot[u], bad);
+    }
   }
   reduce_shift_edges<GT>(x.s, nvec, lane, bad);
 }

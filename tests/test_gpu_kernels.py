@@ -116,6 +116,23 @@ def test_reduce_shifted_loads(ss, N, n, accumulate):
     assert flag.item() == 0
 
 
+@pytest.mark.parametrize("N", [2, 3, 8, 9, 65])
+def test_reduce_mixed_phases_some_aligned(ss, N):
+    """Rank r's view r % 8 elements into its buffer: rank 0 (and 8, 16, ...) at the output's phase,
+    the others each at its own -- the warp-cooperative mixed-phase reduce with some ranks needing no
+    shift; bit-exact against the oracle, accumulating with a post scale."""
+    import torch
+    n = 200_003
+    specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 9) for r in range(N)]
+    G = [dev_bits(s, n, offset=r % 8) for r, s in enumerate(specs)]
+    init = dev_bits(synth.normal(1e-2, synth.FP32, synth.MOM1), n)
+    out = init.clone()
+    ss.ss_grad_reduce(G, n, out, post_scale=0.5, accumulate=True)
+    acc = bits_of(init).copy()
+    oracle.grad_reduce([host_bits(s, n) for s in specs], synth.BF16, post_scale=0.5, accumulate_into=acc)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), acc.view(np.uint32))
+
+
 @pytest.mark.parametrize("N", [2, 3, 4, 5, 7, 8, 9, 16, 64, 65])
 @pytest.mark.parametrize("n", [1001, 300_007])
 @pytest.mark.parametrize("accumulate", [True, False])
