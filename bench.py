@@ -722,20 +722,25 @@ def run_suite(args, device) -> dict:
                                      (2 * N + 4 + 4 * accum) * m7)
         out[key] = by_ranks
         del G
-    # the sum of squares writing g_out, every rank's view one element off g_out's phase
-    if want("grad_sumsq_gout_off_by_one_by_ranks"):
+    # the sum of squares across rank counts: read-only, writing g_out, and writing g_out with every
+    # rank's view one element off g_out's phase
+    for key, off, gout in (("grad_sumsq_by_ranks", 0, False), ("grad_sumsq_gout_by_ranks", 0, True),
+                           ("grad_sumsq_gout_off_by_one_by_ranks", 1, True)):
+        if not want(key):
+            continue
         m7 = n - 7
         G = []
         for r in range(64):
             t = torch.empty(n + 8, dtype=torch.bfloat16, device=device)
             synth.device_fill(synth.normal(1e-3, synth.BF16, synth.GRAD, r, 1), t.view(torch.int16))
-            G.append(t[1:1 + m7])
+            G.append(t[off:off + m7])
         by_ranks = {}
         for N in (1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 64):
             Gn = G[:N]
-            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_sumsq(m7, acc, ws, rank_grads=Gn, g_out=g32[:m7])),
-                                     (2 * N + 4) * m7)
-        out["grad_sumsq_gout_off_by_one_by_ranks"] = by_ranks
+            go = g32[:m7] if gout else None
+            by_ranks[str(N)] = entry(timed(lambda: ss.ss_grad_sumsq(m7, acc, ws, rank_grads=Gn, g_out=go)),
+                                     (2 * N + 4 * gout) * m7)
+        out[key] = by_ranks
         del G
     # the fused step across the rank counts between (kernel forms and prefetch thresholds)
     if want("adam_step_by_ranks"):

@@ -162,6 +162,25 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
   s = {t.hi, s.lo + t.lo};
 }
 
+// Minimum resident blocks per SM asked of the compiler: none (0), which leaves
+// the register count to ptxas, except for the realigned-g_out instances of the
+// rank counts in SS_SUMSQ_SHUFFLE_TWO_BLOCKS (bit N: N ranks), which ask for 2.
+// An explicit 1 is not the same as none: with __launch_bounds__(256, 1) ptxas
+// gave the general tiles 147 registers (one block per SM; measured on GB300 at
+// 2^26 elements, 64 ranks, 0.76 of the copy peak) where plain
+// __launch_bounds__(256) gives 124 (two blocks; 1.00). Two blocks measured, for
+// g_out one element off the inputs' phase: 1 rank 0.70 -> 0.75, 3 ranks 0.81 ->
+// 0.88, 4 ranks 0.90 -> 0.85, 2 and 5-8 ranks within 1%.
+#ifndef SS_SUMSQ_SHUFFLE_TWO_BLOCKS
+#define SS_SUMSQ_SHUFFLE_TWO_BLOCKS ((1u << 1) | (1u << 3))
+#endif
+// The general tiles (any rank count) write an off-phase g_out element by element
+// (measured against realigned stores there: 9 / 16 / 64 ranks 0.53 / 0.73 / 0.85
+// of the copy peak against 0.50 / 0.68 / 0.73).
+constexpr int sumsq_min_blocks(int nr, int gout) {
+  return gout == kGoutShuffle && nr > 0 && ((SS_SUMSQ_SHUFFLE_TWO_BLOCKS >> nr) & 1u) ? 2 : 0;
+}
+
 // Tiles of the compile-time rank count NR (1..8), 16-byte vectors: a block's
 // tiles form one stream of load batches (kB groups x NR ranks per batch),
 // double-buffered in registers -- the loads of batch i+1 are in flight while
@@ -169,34 +188,9 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
 // tile is in flight across the tile's block reduction. Batches past the end
 // (of the shard or of the block's tiles) read group 0 instead, always in
 // range, and are dropped, so no branch stands between the loads.
-// With g_out realigned between lanes the stores' shuffles need registers: 1
-// group per batch from 4 ranks on, and at least 2 blocks per SM (<= 128
-// registers). Measured on GB300 at 2^26 elements, gradients one element off
-// g_out's phase: 8 ranks at one block per SM (132 registers) 0.83 of the copy
-// peak, at three (79, 1 group a batch) 0.88; 5-7 ranks 0.89-0.93 at two blocks,
-// 0.88 at three; 2-3 ranks 0.82 / 0.88 at two blocks with 4 / 2 groups a batch,
-// 0.80-0.81 at three with 2.
-#ifndef SS_SUMSQ_SHUFFLE_MAX_KB
-#define SS_SUMSQ_SHUFFLE_MAX_KB 4
-#endif
-#ifndef SS_SUMSQ_SHUFFLE_MIN_BLOCKS
-#define SS_SUMSQ_SHUFFLE_MIN_BLOCKS 2
-#endif
-// The general tiles (any rank count) write an off-phase g_out realigned between
-// lanes as the ranked tiles do (measured 9 / 16 / 64 ranks 0.51 / 0.69 / 0.73 of
-// the copy peak, against 0.42 / 0.60 / 0.72 element by element), or, with
-// SS_SUMSQ_GENERAL_SHUFFLE 0, element by element.
-#ifndef SS_SUMSQ_GENERAL_SHUFFLE
-#define SS_SUMSQ_GENERAL_SHUFFLE 1
-#endif
-#ifndef SS_SUMSQ_GENERAL_MIN_BLOCKS
-#define SS_SUMSQ_GENERAL_MIN_BLOCKS 1
-#endif
 template <int GT, int MAXR, int NR, int GOUT>
 __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, float2* red, bool& bad) {
-  constexpr int kB0 = NR == 2 ? 4 : (NR <= 4 ? 2 : 1);  // groups per batch (measured best on GB300)
-  constexpr int kBs = NR >= 4 ? 1 : SS_SUMSQ_SHUFFLE_MAX_KB;  // realigned g_out: fit 80 registers
-  constexpr int kB = GOUT == kGoutShuffle && kB0 > kBs ? kBs : kB0;
+  constexpr int kB = NR == 2 ? 4 : (NR <= 4 ? 2 : 1);  // groups per batch (measured best on GB300)
   static_assert(kSumsqGroups % (2 * kB) == 0, "two batches per pipeline round");
   const int64_t nvec = (a.n - a.head) / kGroup;
   const int64_t stride = static_cast<int64_t>(gridDim.x);
@@ -256,9 +250,7 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
 // gradient, or element-wise access -- each thread issues its tile's loads
 // group by group, then squares and sums them.
 template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR, int GOUT = kGoutVec>
-__global__ void __launch_bounds__(kThreads, GOUT == kGoutShuffle ? (NR > 0 ? SS_SUMSQ_SHUFFLE_MIN_BLOCKS
-                                                                         : SS_SUMSQ_GENERAL_MIN_BLOCKS)
-                                                                : 1)
+__global__ void __launch_bounds__(kThreads, sumsq_min_blocks(NR, GOUT))
     sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
   __shared__ float2 red[2 * (kThreads / 32)];
   pdl_wait();
@@ -398,7 +390,7 @@ ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtyp
   };
   const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
   constexpr int kRanked = SH ? kGoutShuffle : kGoutVec;
-  constexpr int kGeneral = SH ? (SS_SUMSQ_GENERAL_SHUFFLE ? kGoutShuffle : kGoutElem) : kGoutVec;
+  constexpr int kGeneral = SH ? kGoutElem : kGoutVec;
 #define SS_SUMSQ_NR(G, R) \
   case R: go(sumsq_tiles_kernel<G, false, true, MAXR, R, kRanked>); break;
 // The per-rank-count forms exist for the small rank table only (at most 8 ranks),
