@@ -4,7 +4,8 @@ n = 2^31 + 7 elements, N = 2 bf16 ranks (about 39 GB on the device): one fused s
 sampled elements (both ends, runs around 2^31 and random points) against the oracle; then the
 16-bit parameters unsharded with a 2^31 + 7-element shard and a small one, checked the same way;
 and the same step with both ranks' gradient views one element off the state's 16-byte phase (the
-warp-cooperative shifted-load kernel, whose run and group indices then pass 2^31 too).
+warp-cooperative shifted-load kernel, whose run and group indices then pass 2^31 too); and one
+rank's gradient accumulated into an fp32 output of 2^31 + 7 elements, aligned and one element off.
 """
 import numpy as np
 import pytest
@@ -101,4 +102,30 @@ def test_shifted_step_beyond_2_31_elements(ss):
         assert_state_close(t[it].cpu().numpy(), r, name)
     assert_p16_within_ulp(p16.view(torch.int16)[it].cpu().numpy().view(np.uint16), rp, oracle.BF16, "p16")
     del G, master, m, v, p16
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("off", [0, 1])
+def test_one_rank_reduce_beyond_2_31_elements(ss, off):
+    """One rank's gradient accumulated into the fp32 output, n = 2^31 + 7: aligned (the 4-element
+    lane map) or the view one element off the output's phase (several runs a warp at a time, the
+    sums stored through shared memory); bit-exact against the oracle on sampled elements."""
+    import torch
+    n = N_LARGE
+    spec = synth.normal(1e-3, synth.BF16, synth.GRAD, 0, 7)
+    base = torch.empty(n + 8, dtype=torch.bfloat16, device="cuda")
+    g = base[off:off + n]
+    synth.device_fill(spec, g.view(torch.int16))
+    ospec = synth.normal(1e-2, synth.FP32, synth.MOM1)
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    synth.device_fill(ospec, out.view(torch.int32))
+    ss.ss_grad_reduce([g], n, out, post_scale=0.5, accumulate=True)
+    torch.cuda.synchronize()
+    idx = np.unique(np.concatenate([sample_indices(0, n, 200_000, 8),
+                                    np.arange((1 << 31) - 40, (1 << 31) + 7)]))
+    acc = synth.host_gather(ospec, idx).view(np.float32).copy()
+    oracle.grad_reduce([synth.host_gather(spec, idx)], oracle.BF16, post_scale=0.5, accumulate_into=acc)
+    it = torch.from_numpy(idx.astype(np.int64)).cuda()
+    assert np.array_equal(out[it].cpu().numpy().view(np.uint32), acc.view(np.uint32))
+    del base, out
     torch.cuda.empty_cache()
