@@ -613,6 +613,9 @@ def run_suite(args, device) -> dict:
         out["adam_step_fp32_grad"] = entry(timed(lambda: ss.ss_adam_step(hp, n, *st, g32=g32, param16=p16)), 30 * n)
     ws = torch.empty(max(ss.ss_grad_sumsq_workspace(n) // 8, 1), dtype=torch.float64, device=device)
     acc = torch.empty(1, dtype=torch.float64, device=device)
+    if want("grad_sumsq_fp32_grad"):
+        # the clip pass over an fp32 gradient (accumulated micro-batches), before a step from g32
+        out["grad_sumsq_fp32_grad"] = entry(timed(lambda: ss.ss_grad_sumsq(n, acc, ws, g32=g32)), 4 * n)
     extra8 = ("adam_step_N8_grads_off_by_one", "grad_reduce_accumulate_N8", "adam_step_N8_fp16_unscale_flag_skip",
               "adam_step_N8_param16_into_flat")
     for N in (2, 8, 64):
