@@ -93,13 +93,14 @@ __global__ void __launch_bounds__(CHUNKED ? kReduceChunkThreads : kThreads) redu
 // copy peak; accumulating, 1 / 2 / 3 ranks 0.87 / 0.95 / 0.99 -> 0.93 / 1.01 /
 // 1.02; without accumulating 2 and 3 ranks measured slower (0.90 / 0.93 against
 // 0.95 / 1.01: the halved gradient loads), 4 ranks the same.
-#ifndef SS_RED_QUAD_RANKS
-#define SS_RED_QUAD_RANKS 1  // up to this many ranks, not accumulating
+// Which rank counts (bit N: N ranks, 1-4) take it, not accumulating and accumulating.
+#ifndef SS_RED_QUAD_MASK
+#define SS_RED_QUAD_MASK (1u << 1)
 #endif
-#ifndef SS_RED_QUAD_ACC_RANKS
-#define SS_RED_QUAD_ACC_RANKS 3  // up to this many ranks, accumulating
+#ifndef SS_RED_QUAD_ACC_MASK
+#define SS_RED_QUAD_ACC_MASK ((1u << 2) | (1u << 3))
 #endif
-static_assert(SS_RED_QUAD_RANKS <= 4 && SS_RED_QUAD_ACC_RANKS <= 4, "quad forms exist for 1-4 ranks");
+static_assert(((SS_RED_QUAD_MASK | SS_RED_QUAD_ACC_MASK) & ~0x1Eu) == 0, "quad forms exist for 1-4 ranks");
 template <int GT, int MAXR, int NR, bool ACC>
 __global__ void __launch_bounds__(kReduceChunkThreads) reduce_quad_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
   __shared__ unsigned next_chunk;
@@ -176,13 +177,113 @@ bool reduce_quad(const ReduceArgs<MAXR>& a, ss_status& st, void* stream) {
   } else {
 #define SS_RED_QUAD(R)                                                                                       \
   if (a.n_ranks == R) {                                                                                      \
-    if constexpr (SS_RED_QUAD_ACC_RANKS >= R)                                                                \
+    if constexpr ((SS_RED_QUAD_ACC_MASK >> R) & 1u)                                                          \
       if (a.accumulate) return st = launch_reduce_quad<G, MAXR, R, true>(a, stream), true;                   \
-    if constexpr (SS_RED_QUAD_RANKS >= R)                                                                    \
+    if constexpr ((SS_RED_QUAD_MASK >> R) & 1u)                                                              \
       if (!a.accumulate) return st = launch_reduce_quad<G, MAXR, R, false>(a, stream), true;                 \
   }
     SS_RED_QUAD(1) SS_RED_QUAD(2) SS_RED_QUAD(3) SS_RED_QUAD(4)
 #undef SS_RED_QUAD
+    return false;
+  }
+}
+
+// The chunked form with the rank count and accumulation fixed at compile time,
+// each warp's sums stored through shared memory as consecutive 16-byte vectors
+// (vector f of a chunk holds elements 4f..4f+3 of its 32 groups) and, when
+// accumulating, the old values loaded in that layout with the gradients. It
+// keeps the 16-byte gradient loads that the quad form halves. Measured on
+// GB300 at 2^26 elements against the quad and chunked forms: 2 ranks 0.95 ->
+// 0.96-0.97, 1 rank accumulating 0.93 -> 0.99-1.00; 2-3 ranks accumulating
+// 0.97 / 1.02 against the quad form's 1.01 / 1.03; 3-8 ranks within 1%.
+#ifndef SS_RED_VEC_TX_MASK
+#define SS_RED_VEC_TX_MASK (1u << 2)  // bit N: N ranks (1-8), not accumulating
+#endif
+#ifndef SS_RED_VEC_TX_ACC_MASK
+#define SS_RED_VEC_TX_ACC_MASK (1u << 1)  // the same, accumulating
+#endif
+template <int GT, int MAXR, int NR, bool ACC>
+__global__ void __launch_bounds__(kReduceChunkThreads) reduce_vec_tx_kernel(const __grid_constant__ ReduceArgs<MAXR> a) {
+  __shared__ unsigned next_chunk;
+  __shared__ float4 tx[kReduceChunkThreads / 32][64];
+  if (threadIdx.x == 0) next_chunk = 0;
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  const int64_t nvec = (a.n - a.head) / kGroup;
+  const int lane = threadIdx.x & 31;
+  float4* t = tx[threadIdx.x >> 5];
+  const ChunkMap<kReduceChunkThreads / 32> map(nvec);
+  bool bad = false;
+  for (int64_t c = map.take<false>(&next_chunk, lane); c < map.nchunk; c = map.take<false>(&next_chunk, lane)) {
+    const int64_t gi = c * 32 + lane;
+    const int64_t cb = a.head + c * 32 * kGroup;  // the chunk's first element
+    uint4 w[NR];
+    float4 ot[2];
+    if (gi < nvec) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r)
+        w[r] = __ldcs(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.ranks.p[r]) + cb + lane * kGroup));
+    }
+    if (ACC) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int f = lane + 32 * k;
+        if (c * 32 + f / 2 < nvec) ot[k] = __ldcs(reinterpret_cast<const float4*>(a.out + cb + 4 * f));
+      }
+    }
+    float g[8];
+    widen8<GT>(w[0], g);
+#pragma unroll
+    for (int r = 1; r < NR; ++r) add8<GT>(w[r], g);
+    t[2 * lane] = make_float4(g[0], g[1], g[2], g[3]);
+    t[2 * lane + 1] = make_float4(g[4], g[5], g[6], g[7]);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int f = lane + 32 * k;
+      if (c * 32 + f / 2 < nvec) {
+        float4 v = t[f];
+        if (a.post_scale != 1.0f) {
+          v.x = v.x * a.post_scale; v.y = v.y * a.post_scale; v.z = v.z * a.post_scale; v.w = v.w * a.post_scale;
+        }
+        if (ACC) {
+          v.x = ot[k].x + v.x; v.y = ot[k].y + v.y; v.z = ot[k].z + v.z; v.w = ot[k].w + v.w;
+        }
+        if (a.nonfinite) bad |= !finite(v.x) || !finite(v.y) || !finite(v.z) || !finite(v.w);
+        __stcs(reinterpret_cast<float4*>(a.out + cb + 4 * f), v);
+      }
+    }
+    __syncwarp();
+  }
+  const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t tail0 = a.head + nvec * kGroup;
+  if (tid < a.head + (a.n - tail0)) reduce_one<GT>(a, tid < a.head ? tid : tail0 + (tid - a.head), bad);
+  if (a.nonfinite) {
+    const unsigned any = __ballot_sync(0xFFFFFFFFu, bad);
+    if (any && lane == 0) *a.nonfinite = 1;
+  }
+}
+
+template <int G, int MAXR>
+bool reduce_vec_tx(const ReduceArgs<MAXR>& a, ss_status& st, void* stream) {
+  if constexpr (MAXR != kSmallRanks || (SS_RED_VEC_TX_MASK | SS_RED_VEC_TX_ACC_MASK) == 0) {
+    return false;
+  } else {
+    auto go = [&](auto* fn) {
+      st = launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kReduceChunkThreads), a,
+                  stream, kReduceChunkThreads);
+      return true;
+    };
+#define SS_RED_TX(R)                                                                                          \
+  if (a.n_ranks == R) {                                                                                       \
+    if constexpr ((SS_RED_VEC_TX_ACC_MASK >> R) & 1u)                                                         \
+      if (a.accumulate) return go(reduce_vec_tx_kernel<G, MAXR, R, true>);                                    \
+    if constexpr ((SS_RED_VEC_TX_MASK >> R) & 1u)                                                             \
+      if (!a.accumulate) return go(reduce_vec_tx_kernel<G, MAXR, R, false>);                                  \
+  }
+    SS_RED_TX(1) SS_RED_TX(2) SS_RED_TX(3) SS_RED_TX(4) SS_RED_TX(5) SS_RED_TX(6) SS_RED_TX(7) SS_RED_TX(8)
+#undef SS_RED_TX
     return false;
   }
 }
@@ -575,6 +676,7 @@ ss_status run_reduce(const ReduceArgs<MAXR>& a, bool vec, ss_dtype gt, void* str
   if (gt == G) {                                                                           \
     ss_status st = SS_OK;                                                                  \
     if (vec && reduce_quad<G>(a, st, stream)) return st;                                   \
+    if (vec && reduce_vec_tx<G>(a, st, stream)) return st;                                 \
     if (vec && a.n_ranks <= kReduceChunkRanks) {                                           \
       auto* fn = reduce_vec_kernel<G, MAXR, true>;                                         \
       return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (a.n - a.head) / kGroup, kReduceChunkThreads), \

@@ -108,8 +108,8 @@ def test_step_from_fp32_gradient_writes_only_its_arrays(ss):
 
 
 REDUCE_FORMS = [  # (N, gradient view offset of rank r, output offset)
-    (1, lambda r: 0, 0),             # vector, 4 + 4 elements a lane at lane stride
-    (2, lambda r: 0, 0),             # vector, 8 elements a lane (accumulating: 4 + 4)
+    (1, lambda r: 0, 0),             # vector: 4 + 4 elements a lane (accumulating: stored through shared memory)
+    (2, lambda r: 0, 0),             # vector: stored through shared memory (accumulating: 4 + 4 a lane)
     (4, lambda r: 0, 0),             # vector, chunked
     (16, lambda r: 0, 0),            # vector, grid-stride
     (1, lambda r: 1, 0),             # shifted, four runs a warp at a time

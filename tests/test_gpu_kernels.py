@@ -311,9 +311,9 @@ def test_step_chunk_boundaries(ss, N, from_g32, k, d):
 @pytest.mark.parametrize("k,d", [(1, -1), (1, 0), (2, 257), (3, -4096)])
 def test_reduce_chunk_boundaries(ss, N, accumulate, k, d):
     """The aligned reduce around whole passes of its grid (one 1024-thread block per SM whose 32
-    warps take chunks of 256 elements: 8 elements a lane, or, for 1 rank and for 1-3 ranks
-    accumulating, 4 + 4 at lane stride; 9 ranks grid-stride), accumulating into the output or not:
-    bit-exact, so no element is added twice or missed."""
+    warps take chunks of 256 elements -- 8 elements a lane, 4 + 4 at lane stride, or 8 a lane stored
+    through shared memory, by rank count and accumulation; 9 ranks grid-stride), accumulating into
+    the output or not: bit-exact, so no element is added twice or missed."""
     import torch
     n = k * _sms() * 32 * 32 * 8 + d
     specs = [synth.normal(1e-3, synth.BF16, synth.GRAD, r, 4) for r in range(N)]
