@@ -121,21 +121,39 @@ __device__ __forceinline__ void store_g_out_shifted(float* out, const float (&g)
 }
 
 // How g_out is written: as 16-byte vectors at the inputs' phase, realigned
-// between lanes by store_g_out_shifted (g_out 1-3 floats off that phase), or
-// element by element.
-enum GoutStore : int { kGoutVec = 0, kGoutShuffle = 1, kGoutElem = 2 };
+// between lanes by store_g_out_shifted (g_out 1-3 floats off that phase),
+// element by element, or staged: the warp's 32 consecutive groups pass through
+// 1 KB of shared memory and are stored as consecutive 16-byte vectors, each
+// instruction covering 512 bytes (where each lane storing its own group leaves
+// every instruction half of each 32-byte sector it touches).
+enum GoutStore : int { kGoutVec = 0, kGoutShuffle = 1, kGoutElem = 2, kGoutStaged = 3 };
 
 // One reduced group of 8 values at element e: optionally stored to g_out, its
 // squares added in fp32 (a fixed FMA chain), and the sum added to the thread's
 // fp32 pair. The finiteness test runs per element only when the group's sum is
 // not finite (a non-finite value, or squares past the fp32 range). With
-// kGoutShuffle all lanes of the warp call it, `valid` telling which hold a
-// group; otherwise only lanes holding a group call it.
+// kGoutShuffle and kGoutStaged all lanes of the warp call it, `valid` telling
+// which hold a group (kGoutStaged: `stage` is the warp's 64 float4 slots and
+// `warp_valid` the number of the warp's groups in the shard); otherwise only
+// lanes holding a group call it.
 template <bool VEC, int GOUT, int MAXR>
 __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e, const float (&g)[8], dd& s,
-                                            bool& bad, bool valid = true, bool next_valid = true) {
+                                            bool& bad, bool valid = true, bool next_valid = true,
+                                            float4* stage = nullptr, int warp_valid = 0) {
   if (a.g_out) {
-    if constexpr (GOUT == kGoutShuffle) {
+    if constexpr (GOUT == kGoutStaged) {
+      const int lane = threadIdx.x & 31;
+      stage[2 * lane] = make_float4(g[0], g[1], g[2], g[3]);
+      stage[2 * lane + 1] = make_float4(g[4], g[5], g[6], g[7]);
+      __syncwarp();
+      float* ew = a.g_out + e - kGroup * lane;  // the warp's first group (consecutive groups)
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int f = lane + 32 * k;
+        if (f / 2 < warp_valid) __stcs(reinterpret_cast<float4*>(ew) + f, stage[f]);
+      }
+      __syncwarp();
+    } else if constexpr (GOUT == kGoutShuffle) {
       switch ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) >> 2) {  // the same for every group
         case 1: store_g_out_shifted<1>(a.g_out + e, g, valid, next_valid); break;
         case 2: store_g_out_shifted<2>(a.g_out + e, g, valid, next_valid); break;
@@ -148,7 +166,7 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
       for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
     }
   }
-  if constexpr (GOUT == kGoutShuffle) {
+  if constexpr (GOUT == kGoutShuffle || GOUT == kGoutStaged) {
     if (!valid) return;
   }
   float c = 0.0f;
@@ -189,7 +207,8 @@ constexpr int sumsq_min_blocks(int nr, int gout) {
 // (of the shard or of the block's tiles) read group 0 instead, always in
 // range, and are dropped, so no branch stands between the loads.
 template <int GT, int MAXR, int NR, int GOUT>
-__device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, float2* red, bool& bad) {
+__device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, float2* red, bool& bad,
+                                                   float4* stage) {
   constexpr int kB = NR == 2 ? 4 : (NR <= 4 ? 2 : 1);  // groups per batch (measured best on GB300)
   static_assert(kSumsqGroups % (2 * kB) == 0, "two batches per pipeline round");
   const int64_t nvec = (a.n - a.head) / kGroup;
@@ -218,9 +237,15 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
         for (int j = 0; j < 8; ++j) g[j] = g[j] * a.post_scale;
       }
       const int64_t gq = g0 + (q0 + b) * kThreads;
-      if constexpr (GOUT == kGoutShuffle)
+      if constexpr (GOUT == kGoutShuffle) {
         sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad, gq < nvec, gq + 1 < nvec);
-      else if (gq < nvec) sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad);
+      } else if constexpr (GOUT == kGoutStaged) {
+        const int64_t left = nvec - (gq - (threadIdx.x & 31));  // groups of the warp's 32 in the shard
+        sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad, gq < nvec, true, stage,
+                                static_cast<int>(left < 0 ? 0 : (left > 32 ? 32 : left)));
+      } else if (gq < nvec) {
+        sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad);
+      }
     }
   };
   int64_t tile = blockIdx.x;
@@ -253,12 +278,13 @@ template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR, int GOUT = kGoutVec
 __global__ void __launch_bounds__(kThreads, sumsq_min_blocks(NR, GOUT))
     sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
   __shared__ float2 red[2 * (kThreads / 32)];
+  __shared__ float4 stage[GOUT == kGoutStaged ? (kThreads / 32) * 64 : 1];
   pdl_wait();
   pdl_trigger();  // the slot sum may be scheduled now; it waits for this grid to finish
   const int64_t nvec = (a.n - a.head) / kGroup;
   bool bad = false;
   if constexpr (VEC && !FROM_G32 && NR > 0) {
-    sumsq_ranked_tiles<GT, MAXR, NR, GOUT>(a, red, bad);
+    sumsq_ranked_tiles<GT, MAXR, NR, GOUT>(a, red, bad, stage + (GOUT == kGoutStaged ? (threadIdx.x >> 5) * 64 : 0));
   } else {
     int it = 0;
     for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
@@ -377,6 +403,14 @@ __global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, fl
 // one element off: 2 ranks 0.82 of the copy peak against 0.29 element by element, 8 ranks
 // 0.91 against 0.72), the general tiles write it element by element (64 ranks: 0.87,
 // against 0.72 realigned).
+// The per-rank-count tiles writing g_out at the inputs' phase stage it (bit N: N
+// ranks). Measured on GB300 at 2^26 elements against per-lane 16-byte stores, one
+// box: 1 / 2 / 3 ranks 0.75 / 0.83 / 0.84 -> 0.84 / 0.86 / 0.90 of the copy peak,
+// 4-8 ranks 0.90-0.97 -> 0.94-0.98; the results are the same bits. Without g_out
+// the unstaged instances run (the staged ones hold more registers).
+#ifndef SS_SUMSQ_STAGED
+#define SS_SUMSQ_STAGED 0x1FEu
+#endif
 template <int MAXR, bool SH>
 ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
   // One wave: no more blocks than fit on the GPU at once (the kernel's own
@@ -391,8 +425,15 @@ ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtyp
   const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
   constexpr int kRanked = SH ? kGoutShuffle : kGoutVec;
   constexpr int kGeneral = SH ? kGoutElem : kGoutVec;
-#define SS_SUMSQ_NR(G, R) \
-  case R: go(sumsq_tiles_kernel<G, false, true, MAXR, R, kRanked>); break;
+  // g_out at the inputs' phase, for the rank counts in SS_SUMSQ_STAGED: staged stores
+  const bool staged = !SH && a.g_out != nullptr && ((SS_SUMSQ_STAGED >> nr) & 1u);
+#define SS_SUMSQ_NR(G, R)                                                                 \
+  case R:                                                                                 \
+    if (!SH && ((SS_SUMSQ_STAGED >> R) & 1u) && staged)                                   \
+      go(sumsq_tiles_kernel<G, false, true, MAXR, R, SH ? kRanked : kGoutStaged>);        \
+    else                                                                                  \
+      go(sumsq_tiles_kernel<G, false, true, MAXR, R, kRanked>);                           \
+    break;
 // The per-rank-count forms exist for the small rank table only (at most 8 ranks),
 // and an fp32 gradient always travels with the small table.
 #define SS_SUMSQ_RANKED(G)                                                                              \

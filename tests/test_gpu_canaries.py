@@ -141,9 +141,9 @@ def test_reduce_writes_only_its_output(ss, form, n, accumulate):
                                          (4, 3, 0)])
 @pytest.mark.parametrize("n", [37, 100_003])
 def test_sumsq_writes_only_g_out(ss, N, goff, ooff, n):
-    """g_out aligned, 1-3 floats off the gradients' phase (realigned between lanes for the
-    per-rank-count tiles, element by element for the general ones), and the gradients off g_out's
-    phase."""
+    """g_out aligned (staged through shared memory in the per-rank-count tiles), 1-3 floats off the
+    gradients' phase (realigned between lanes for the per-rank-count tiles, element by element for
+    the general ones), and the gradients off g_out's phase."""
     import torch
     G = grads(n, N, lambda r: goff)
     g_out = guarded(n, torch.float32, ooff)
