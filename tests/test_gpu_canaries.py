@@ -5,8 +5,8 @@ into a larger buffer whose elements before and after the view hold a canary bit 
 on ragged lengths with views at offsets that select each kernel form -- aligned double-buffered,
 single-buffered, warp-cooperative shifted (one phase and mixed phases, 512-, 384- and 256-thread
 blocks), per-thread shifted, element-wise, the fp32-gradient form; the reduce's vector and shifted
-forms (one phase and mixed phases); the sum of squares with g_out aligned, realigned between lanes and element by
-element; the copies at and off the shards' phase -- and every canary must be intact afterwards, so no
+forms (one phase and mixed phases); the sum of squares with g_out staged through shared memory,
+realigned between lanes and element by element; the copies at and off the shards' phase -- and every canary must be intact afterwards, so no
 form writes outside its arrays (the head/tail and first/last-group edges included).
 """
 import numpy as np
