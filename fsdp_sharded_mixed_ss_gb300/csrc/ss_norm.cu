@@ -120,13 +120,52 @@ __device__ __forceinline__ void store_g_out_shifted(float* out, const float (&g)
   }
 }
 
+// The same vectors staged through the warp's 64 float4 slots: lane l's two
+// vectors are the warp's consecutive aligned vectors 2l and 2l + 1 (counted from
+// lane 0's first), so after the exchange each store instruction covers 512
+// contiguous bytes. `wv`: the number of the warp's groups in the shard; a vector
+// is stored when the groups it covers are (the others' elements go one by one).
+template <int K>
+__device__ __forceinline__ void store_g_out_shifted_staged(float* out, const float (&g)[8], bool valid,
+                                                           float4* t, int wv) {
+  static_assert(K >= 1 && K <= 3, "an fp32 array is 1-3 floats off a 16-byte boundary");
+  const int lane = threadIdx.x & 31;
+  float nx[4 - K];
+#pragma unroll
+  for (int j = 0; j < 4 - K; ++j) nx[j] = __shfl_down_sync(0xFFFFFFFFu, g[j], 1);
+  float w[4];
+#pragma unroll
+  for (int j = 0; j < K; ++j) w[j] = g[8 - K + j];
+#pragma unroll
+  for (int j = 0; j < 4 - K; ++j) w[K + j] = nx[j];
+  t[2 * lane] = make_float4(g[4 - K], g[5 - K], g[6 - K], g[7 - K]);
+  t[2 * lane + 1] = make_float4(w[0], w[1], w[2], w[3]);
+  __syncwarp();
+  float4* base = reinterpret_cast<float4*>(out - kGroup * lane + 4 - K);  // lane 0's first vector
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int f = lane + 32 * k;
+    const int l = f >> 1;
+    if ((f & 1) ? l + 1 < wv : l < wv) __stcs(base + f, t[f]);
+  }
+  __syncwarp();
+  if (valid && !(lane + 1 < wv)) {
+#pragma unroll
+    for (int j = 0; j < K; ++j) out[8 - K + j] = g[8 - K + j];
+  }
+  if (valid && lane == 0) {
+#pragma unroll
+    for (int j = 0; j < 4 - K; ++j) out[j] = g[j];
+  }
+}
+
 // How g_out is written: as 16-byte vectors at the inputs' phase, realigned
 // between lanes by store_g_out_shifted (g_out 1-3 floats off that phase),
 // element by element, or staged: the warp's 32 consecutive groups pass through
 // 1 KB of shared memory and are stored as consecutive 16-byte vectors, each
 // instruction covering 512 bytes (where each lane storing its own group leaves
 // every instruction half of each 32-byte sector it touches).
-enum GoutStore : int { kGoutVec = 0, kGoutShuffle = 1, kGoutElem = 2, kGoutStaged = 3 };
+enum GoutStore : int { kGoutVec = 0, kGoutShuffle = 1, kGoutElem = 2, kGoutStaged = 3, kGoutShuffleStaged = 4 };
 
 // One reduced group of 8 values at element e: optionally stored to g_out, its
 // squares added in fp32 (a fixed FMA chain), and the sum added to the thread's
@@ -153,6 +192,12 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
         if (f / 2 < warp_valid) __stcs(reinterpret_cast<float4*>(ew) + f, stage[f]);
       }
       __syncwarp();
+    } else if constexpr (GOUT == kGoutShuffleStaged) {
+      switch ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) >> 2) {  // the same for every group
+        case 1: store_g_out_shifted_staged<1>(a.g_out + e, g, valid, stage, warp_valid); break;
+        case 2: store_g_out_shifted_staged<2>(a.g_out + e, g, valid, stage, warp_valid); break;
+        default: store_g_out_shifted_staged<3>(a.g_out + e, g, valid, stage, warp_valid); break;
+      }
     } else if constexpr (GOUT == kGoutShuffle) {
       switch ((reinterpret_cast<uintptr_t>(a.g_out + e) & 15u) >> 2) {  // the same for every group
         case 1: store_g_out_shifted<1>(a.g_out + e, g, valid, next_valid); break;
@@ -166,7 +211,7 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
       for (int j = 0; j < 8; ++j) a.g_out[e + j] = g[j];
     }
   }
-  if constexpr (GOUT == kGoutShuffle || GOUT == kGoutStaged) {
+  if constexpr (GOUT == kGoutShuffle || GOUT == kGoutStaged || GOUT == kGoutShuffleStaged) {
     if (!valid) return;
   }
   float c = 0.0f;
@@ -181,8 +226,9 @@ __device__ __forceinline__ void sumsq_group(const SumsqArgs<MAXR>& a, int64_t e,
 }
 
 // Minimum resident blocks per SM asked of the compiler: none (0), which leaves
-// the register count to ptxas, except for the realigned-g_out instances of the
-// rank counts in SS_SUMSQ_SHUFFLE_TWO_BLOCKS (bit N: N ranks), which ask for 2.
+// the register count to ptxas, except for the unstaged realigned-g_out instances
+// (rank counts outside SS_SUMSQ_SHUFFLE_STAGED) of the rank counts in
+// SS_SUMSQ_SHUFFLE_TWO_BLOCKS (bit N: N ranks), which ask for 2.
 // An explicit 1 is not the same as none: with __launch_bounds__(256, 1) ptxas
 // gave the general tiles 147 registers (one block per SM; measured on GB300 at
 // 2^26 elements, 64 ranks, 0.76 of the copy peak) where plain
@@ -239,7 +285,7 @@ __device__ __forceinline__ void sumsq_ranked_tiles(const SumsqArgs<MAXR>& a, flo
       const int64_t gq = g0 + (q0 + b) * kThreads;
       if constexpr (GOUT == kGoutShuffle) {
         sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad, gq < nvec, gq + 1 < nvec);
-      } else if constexpr (GOUT == kGoutStaged) {
+      } else if constexpr (GOUT == kGoutStaged || GOUT == kGoutShuffleStaged) {
         const int64_t left = nvec - (gq - (threadIdx.x & 31));  // groups of the warp's 32 in the shard
         sumsq_group<true, GOUT>(a, a.head + gq * kGroup, g, s, bad, gq < nvec, true, stage,
                                 static_cast<int>(left < 0 ? 0 : (left > 32 ? 32 : left)));
@@ -278,13 +324,14 @@ template <int GT, bool FROM_G32, bool VEC, int MAXR, int NR, int GOUT = kGoutVec
 __global__ void __launch_bounds__(kThreads, sumsq_min_blocks(NR, GOUT))
     sumsq_tiles_kernel(const __grid_constant__ SumsqArgs<MAXR> a) {
   __shared__ float2 red[2 * (kThreads / 32)];
-  __shared__ float4 stage[GOUT == kGoutStaged ? (kThreads / 32) * 64 : 1];
+  __shared__ float4 stage[GOUT == kGoutStaged || GOUT == kGoutShuffleStaged ? (kThreads / 32) * 64 : 1];
   pdl_wait();
   pdl_trigger();  // the slot sum may be scheduled now; it waits for this grid to finish
   const int64_t nvec = (a.n - a.head) / kGroup;
   bool bad = false;
   if constexpr (VEC && !FROM_G32 && NR > 0) {
-    sumsq_ranked_tiles<GT, MAXR, NR, GOUT>(a, red, bad, stage + (GOUT == kGoutStaged ? (threadIdx.x >> 5) * 64 : 0));
+    sumsq_ranked_tiles<GT, MAXR, NR, GOUT>(
+        a, red, bad, stage + (GOUT == kGoutStaged || GOUT == kGoutShuffleStaged ? (threadIdx.x >> 5) * 64 : 0));
   } else {
     int it = 0;
     for (int64_t tile = blockIdx.x; tile < a.ntiles; tile += gridDim.x, ++it) {
@@ -411,6 +458,14 @@ __global__ void clip_coef_kernel(const double* shard_sumsq, int32_t n_shards, fl
 #ifndef SS_SUMSQ_STAGED
 #define SS_SUMSQ_STAGED 0x1FEu
 #endif
+// Likewise with g_out 1-3 floats off the inputs' phase: the realigned vectors
+// pass through the same slots (store_g_out_shifted_staged). Measured on GB300 at
+// 2^26 elements, gradients one element off g_out's phase, against per-lane
+// realigned stores: 1 / 2 / 3 ranks 0.77 / 0.82 / 0.88 -> 0.87 / 0.87 / 0.90 of
+// the copy peak, 4-5 ranks 0.88-0.90 -> 0.91, 6-8 ranks the same (0.91-0.92).
+#ifndef SS_SUMSQ_SHUFFLE_STAGED
+#define SS_SUMSQ_SHUFFLE_STAGED 0x1FEu
+#endif
 template <int MAXR, bool SH>
 ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtype gt, double* out, void* stream) {
   // One wave: no more blocks than fit on the GPU at once (the kernel's own
@@ -425,14 +480,24 @@ ss_status run_sumsq_t(const SumsqArgs<MAXR>& a, bool vec, bool from_g32, ss_dtyp
   const int nr = (vec && !from_g32 && a.n_ranks <= 8) ? a.n_ranks : 0;
   constexpr int kRanked = SH ? kGoutShuffle : kGoutVec;
   constexpr int kGeneral = SH ? kGoutElem : kGoutVec;
-  // g_out at the inputs' phase, for the rank counts in SS_SUMSQ_STAGED: staged stores
-  const bool staged = !SH && a.g_out != nullptr && ((SS_SUMSQ_STAGED >> nr) & 1u);
+  // g_out given, for the rank counts in SS_SUMSQ_STAGED (g_out at the inputs' phase) or
+  // SS_SUMSQ_SHUFFLE_STAGED (off it): staged stores
+  constexpr unsigned kStagedMask = SH ? SS_SUMSQ_SHUFFLE_STAGED : SS_SUMSQ_STAGED;
+  constexpr int kStaged = SH ? kGoutShuffleStaged : kGoutStaged;
+  const bool staged = a.g_out != nullptr && ((kStagedMask >> nr) & 1u);  // SH: g_out is given
 #define SS_SUMSQ_NR(G, R)                                                                 \
   case R:                                                                                 \
-    if (!SH && ((SS_SUMSQ_STAGED >> R) & 1u) && staged)                                   \
-      go(sumsq_tiles_kernel<G, false, true, MAXR, R, SH ? kRanked : kGoutStaged>);        \
-    else                                                                                  \
+    if constexpr (SH && ((kStagedMask >> R) & 1u)) {                                      \
+      go(sumsq_tiles_kernel<G, false, true, MAXR, R, kStaged>);                           \
+    } else {                                                                              \
+      if constexpr ((kStagedMask >> R) & 1u) {                                            \
+        if (staged) {                                                                     \
+          go(sumsq_tiles_kernel<G, false, true, MAXR, R, kStaged>);                       \
+          break;                                                                          \
+        }                                                                                 \
+      }                                                                                   \
       go(sumsq_tiles_kernel<G, false, true, MAXR, R, kRanked>);                           \
+    }                                                                                     \
     break;
 // The per-rank-count forms exist for the small rank table only (at most 8 ranks),
 // and an fp32 gradient always travels with the small table.
