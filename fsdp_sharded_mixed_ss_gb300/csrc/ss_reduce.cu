@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) reduce_scalar_kernel(const __grid_co
 //    0.88 with U = 2 (0.83 with U = 4) -> 0.94; accumulating 0.87-0.88 ->
 //    0.92-0.93. 3-4 ranks measured slower this way (0.93 against 0.94-0.99; the
 //    contiguous stores in the any-rank form cost 3-5% there) and take the
-//    any-rank form.
+//    any-rank form, except 3 ranks at mixed phases not accumulating.
 //  * 7-8 ranks at one phase: register double-buffered (the next run's loads
 //    issued before the current run is summed and stored), one 512-thread block
 //    per SM. At mixed phases 8 ranks measured 0.87 there, so they take the
@@ -635,7 +635,18 @@ ss_status launch_reduce_shift(const ShiftReduceArgs<MAXR>& x, void* stream) {
         if constexpr (SS_RED_BATCH_MAX_RANKS >= 2) return launch_reduce_shift_batch<G, MAXR, 2, MIXED>(x, runs, stream);
         break;
       case 3:
-        if constexpr (SS_RED_BATCH_MAX_RANKS >= 3) return launch_reduce_shift_batch<G, MAXR, 3, MIXED>(x, runs, stream);
+        if constexpr (SS_RED_BATCH_MAX_RANKS >= 3) {
+          return launch_reduce_shift_batch<G, MAXR, 3, MIXED>(x, runs, stream);
+        } else if constexpr (MIXED) {
+          // 3 ranks at mixed phases, not accumulating: the batched form (0.94-0.95 of the copy
+          // peak against 0.89 in the any-rank form; one phase and accumulating it measured slower)
+          if (!a.accumulate) {
+            auto* fn = reduce_shift_batch_kernel<G, MAXR, 3, false, true>;
+            const int64_t u = reduce_batch_runs(3, false);
+            return launch(fn, grid_for(reinterpret_cast<const void*>(fn), (runs + u - 1) / u * 32, kReduceChunkThreads),
+                          x, stream, kReduceChunkThreads);
+          }
+        }
         break;
       case 4:
         if constexpr (SS_RED_BATCH_MAX_RANKS >= 4) return launch_reduce_shift_batch<G, MAXR, 4, MIXED>(x, runs, stream);

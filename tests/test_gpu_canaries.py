@@ -117,7 +117,8 @@ REDUCE_FORMS = [  # (N, gradient view offset of rank r, output offset)
     (6, lambda r: 1, 0),             # shifted, batches of rank chunks
     (8, lambda r: 5, 0),             # shifted, double-buffered
     (8, lambda r: 0, 3),             # the output off the ranks' phase
-    (4, lambda r: (r % 7) + 1, 0),   # mixed phases, two runs at a time
+    (3, lambda r: (r % 7) + 1, 0),   # mixed phases, two runs at a time (accumulating: batches of rank chunks)
+    (4, lambda r: (r % 7) + 1, 0),   # mixed phases, batches of rank chunks
     (8, lambda r: (r % 7) + 1, 0),   # mixed phases, double-buffered
     (12, lambda r: (r % 7) + 1, 0),  # mixed phases, batches of rank chunks
     (4, lambda r: (r % 7) + 1, 1),   # mixed phases, the output one float past a boundary (3 head elements)
