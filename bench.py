@@ -707,7 +707,7 @@ def run_suite(args, device) -> dict:
     for key, offset, accum, ranks in (
             ("grad_reduce_by_ranks", lambda r: 0, False, (1, 2, 3, 4, 6, 8, 16)),
             ("grad_reduce_accumulate_by_ranks", lambda r: 0, True, (1, 2, 3, 4, 8)),
-            ("grad_reduce_off_by_one_by_ranks", lambda r: 1, False, (1, 2, 3, 4, 5, 6, 7, 8, 9, 16)),
+            ("grad_reduce_off_by_one_by_ranks", lambda r: 1, False, (1, 2, 3, 4, 5, 6, 7, 8, 9, 16, 64)),
             ("grad_reduce_accumulate_off_by_one_by_ranks", lambda r: 1, True, (1, 2, 3, 4, 6, 8, 16)),
             ("grad_reduce_mixed_phase_by_ranks", lambda r: (r % 7) + 1, False, (2, 3, 4, 6, 8, 12, 16, 64))):
         if not want(key):
