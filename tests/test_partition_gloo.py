@@ -19,7 +19,7 @@ import pytest
 import torch.multiprocessing as mp
 
 # a unit whose P is not a multiple of the rank counts: shards of unequal length, odd offsets
-NUMELS = [1001, 37, 4099, 64 * 33, 6]   # P = 7255: odd, and not a multiple of 3
+NUMELS = [1001, 37, 4099, 64 * 33, 6]   # P = 7255: odd, and not a multiple of 3, 4 or 7
 HP = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1)
 
 
@@ -88,7 +88,7 @@ def _run(world):
     return dict(out)
 
 
-@pytest.mark.parametrize("world", [2, 3])
+@pytest.mark.parametrize("world", [2, 3, 4, 7])
 def test_partition_exchanges_compose_into_the_virtual_rank_unit(world):
     import oracle
     import synth
