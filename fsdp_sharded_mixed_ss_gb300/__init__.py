@@ -68,6 +68,9 @@ class _Options(ctypes.Structure):
                 ("dev_grad_scale", ctypes.c_void_p), ("dev_skip_flag", ctypes.c_void_p)]
 
 
+_NO_OPTIONS = _Options(None, None, None, None)
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is not built; run `python fsdp_sharded_mixed_ss_gb300/_build.py` "
@@ -108,15 +111,23 @@ def lib():
 
 _torch = None
 _DTYPES = None
+_RAW_STREAM = None
+_GET_DEVICE = None
 
 
 def _t():
-    global _torch, _DTYPES
+    global _torch, _DTYPES, _RAW_STREAM, _GET_DEVICE
     if _torch is None:
         import torch
 
         _torch = torch
         _DTYPES = {torch.bfloat16: SS_BF16, torch.float16: SS_FP16, torch.float32: SS_FP32}
+        # torch's own C entry points for the current device and the current stream's handle
+        # (public equivalents are used when a torch build lacks them)
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        _GET_DEVICE = getattr(torch._C, "_cuda_getDevice", None)
+        if _RAW_STREAM is None or _GET_DEVICE is None:
+            _RAW_STREAM = _GET_DEVICE = None
     return _torch
 
 
@@ -140,6 +151,10 @@ def _stream(stream, like=None) -> int | None:
         return stream if isinstance(stream, int) else stream.cuda_stream
     torch = _t()
     dev = like.device if (like is not None and not isinstance(like, int) and like.is_cuda) else None
+    if _RAW_STREAM is not None:
+        # the current stream's handle without building a torch Stream object (a few microseconds
+        # per call, which small shards feel)
+        return _RAW_STREAM(dev.index if dev is not None and dev.index is not None else _GET_DEVICE())
     return torch.cuda.current_stream(dev).cuda_stream
 
 
@@ -154,7 +169,7 @@ class _DeviceGuard:
         self.ctx = None
         if t is not None and not isinstance(t, int) and t.is_cuda:
             idx = t.device.index
-            if idx is not None and idx != _t().cuda.current_device():
+            if idx is not None and idx != (_GET_DEVICE() if _GET_DEVICE is not None else _t().cuda.current_device()):
                 self.dev = idx
 
     def __enter__(self):
@@ -174,6 +189,11 @@ def _check(rc: int, where: str) -> None:
 
 def _ptr_array(xs) -> array.array:
     """The addresses of xs as a C array of 64-bit pointers (keep it alive across the call)."""
+    if xs and not isinstance(xs[0], int):
+        try:
+            return array.array("Q", [x.data_ptr() for x in xs])
+        except AttributeError:
+            pass
     return array.array("Q", [x if isinstance(x, int) else x.data_ptr() for x in xs])
 
 
@@ -248,7 +268,10 @@ def ss_adam_step(hp: dict, n: int, master, m, v, *, g32=None, rank_grads=None, g
     if param16 is not None and pdtype is None:
         pdtype = _dtype_of(param16)
     ptrs = _ptr_array(ranks) if ranks else None
-    opts = _Options(_ptr(g_out), _ptr(nonfinite_flag), _ptr(dev_grad_scale), _ptr(dev_skip_flag))
+    if g_out is None and nonfinite_flag is None and dev_grad_scale is None and dev_skip_flag is None:
+        opts = _NO_OPTIONS  # read-only for the library
+    else:
+        opts = _Options(_ptr(g_out), _ptr(nonfinite_flag), _ptr(dev_grad_scale), _ptr(dev_skip_flag))
     with _DeviceGuard(master):
         _check(_lib.ss_adam_step(ctypes.byref(h), n, _ptr(g32), _addr(ptrs),
                                  len(ranks), -1 if gdtype is None else gdtype, float(post_scale), _ptr(master), _ptr(m),
